@@ -1,0 +1,93 @@
+// GPU twin of the seeded synthetic-input generator (synth_core.h), used to
+// fill large device-resident inputs (all routed experts of a 40-layer stack
+// are ~200 GB) without staging them through host memory.  Same element
+// definitions as synth.c; K-quant blocks and uniform draws are bit-identical
+// to the host fill, normal draws agree up to the platform log/cos note in
+// synth_core.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "synth_core.h"
+
+namespace {
+
+__global__ void k_fill_q2k(uint8_t* out, uint64_t nblocks, uint64_t block0, uint64_t key,
+                           double dlo, double dhi) {
+  for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < nblocks;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    uint8_t b[84];
+    syn_q2k_block(b, key, block0 + i, dlo, dhi);
+    uint8_t* dst = out + i * 84ULL;   // 4-byte aligned (84 = 4 * 21)
+    for (int k = 0; k < 84; k += 4)
+      *reinterpret_cast<uint32_t*>(dst + k) =
+          (uint32_t)b[k] | ((uint32_t)b[k + 1] << 8) | ((uint32_t)b[k + 2] << 16) | ((uint32_t)b[k + 3] << 24);
+  }
+}
+
+__global__ void k_fill_q3k(uint8_t* out, uint64_t nblocks, uint64_t block0, uint64_t key,
+                           double dlo, double dhi) {
+  for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < nblocks;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    uint8_t b[110];
+    syn_q3k_block(b, key, block0 + i, dlo, dhi);
+    uint8_t* dst = out + i * 110ULL;  // 2-byte aligned (110 = 2 * 55)
+    for (int k = 0; k < 110; k += 2)
+      *reinterpret_cast<uint16_t*>(dst + k) = (uint16_t)((uint32_t)b[k] | ((uint32_t)b[k + 1] << 8));
+  }
+}
+
+__global__ void k_fill_normal_bf16(uint16_t* out, uint64_t n, uint64_t cols, uint64_t key, double std_,
+                                   const double* row_scale) {
+  for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    double s = std_;
+    if (row_scale) s = __dmul_rn(s, row_scale[i / cols]);
+    out[i] = syn_f64_to_bf16(__dmul_rn(syn_normal(key, i), s));
+  }
+}
+
+__global__ void k_fill_uniform_f32(float* out, uint64_t n, uint64_t key, double lo, double hi) {
+  for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n;
+       i += (uint64_t)gridDim.x * blockDim.x)
+    out[i] = __double2float_rn(syn_affine(lo, hi, syn_unit(syn_draw(key, i))));
+}
+
+unsigned grid_for(uint64_t n) {
+  uint64_t g = (n + 255) / 256;
+  if (g > 152ULL * 32ULL) g = 152ULL * 32ULL;
+  return g ? (unsigned)g : 1u;
+}
+
+}  // namespace
+
+extern "C" {
+
+int syn_gpu_fill_q2k(void* out, uint64_t nblocks, uint64_t block0, uint64_t key, double dlo, double dhi,
+                     void* stream) {
+  if (!nblocks) return 0;
+  k_fill_q2k<<<grid_for(nblocks), 256, 0, (cudaStream_t)stream>>>((uint8_t*)out, nblocks, block0, key, dlo, dhi);
+  return (int)cudaGetLastError();
+}
+
+int syn_gpu_fill_q3k(void* out, uint64_t nblocks, uint64_t block0, uint64_t key, double dlo, double dhi,
+                     void* stream) {
+  if (!nblocks) return 0;
+  k_fill_q3k<<<grid_for(nblocks), 256, 0, (cudaStream_t)stream>>>((uint8_t*)out, nblocks, block0, key, dlo, dhi);
+  return (int)cudaGetLastError();
+}
+
+int syn_gpu_fill_normal_bf16(void* out, uint64_t n, uint64_t cols, uint64_t key, double std_,
+                             const double* row_scale_dev, void* stream) {
+  if (!n) return 0;
+  k_fill_normal_bf16<<<grid_for(n), 256, 0, (cudaStream_t)stream>>>((uint16_t*)out, n, cols ? cols : 1, key,
+                                                                    std_, row_scale_dev);
+  return (int)cudaGetLastError();
+}
+
+int syn_gpu_fill_uniform_f32(float* out, uint64_t n, uint64_t key, double lo, double hi, void* stream) {
+  if (!n) return 0;
+  k_fill_uniform_f32<<<grid_for(n), 256, 0, (cudaStream_t)stream>>>(out, n, key, lo, hi);
+  return (int)cudaGetLastError();
+}
+
+}  // extern "C"
