@@ -1,0 +1,132 @@
+"""Python binding of libmoe_v41 (include/moe_v41.h): argument marshalling only.
+
+Every step of the MoE layer runs in the library's sm_103a kernels; this
+module converts torch tensors (device memory) and streams into the C-ABI's
+plain pointers and raises on a non-zero return code.  There is no fallback:
+if the compiled library is missing, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SO = os.path.join(_HERE, "_lib", "libmoe_v41.so")
+
+MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
+MOE_SHARED_BF16, MOE_SHARED_KQUANT = 0, 1
+MOE_OK, MOE_ERR_ARG, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = 0, 1, 2, 3, 4
+MOE_STATUS_NAN_KEY, MOE_STATUS_MISSING_EXPERT, MOE_STATUS_TIMEOUT = 1, 2, 4
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: moe_v41 error {code} ({strerror(code)})")
+        self.code = code
+
+
+class moe_v41_cfg(ctypes.Structure):
+    _fields_ = [("dim", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_routed", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("gate_temp", ctypes.c_float), ("norm_topk_prob", ctypes.c_int32),
+                ("route_scale", ctypes.c_float), ("swiglu_limit", ctypes.c_float), ("max_tokens", ctypes.c_int32),
+                ("path", ctypes.c_int32), ("wait_timeout_us", ctypes.c_uint32)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(SO):
+            raise RuntimeError(f"{SO} is missing: the CUDA library must be built (__graft_entry__.build())")
+        L = ctypes.CDLL(SO)
+        vp, i32, sz, cfgp = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.POINTER(moe_v41_cfg)
+        L.moe_v41_workspace_bytes.restype = sz
+        L.moe_v41_workspace_bytes.argtypes = [cfgp]
+        L.moe_v41_workspace_init.argtypes = [vp, sz, vp]
+        L.moe_v41_quantize_q8_1.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.moe_v41_select_from_logits.argtypes = [cfgp, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.moe_v41_route.argtypes = [cfgp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.moe_v41_forward.argtypes = [cfgp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.moe_v41_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32), i32]
+        L.moe_v41_strerror.restype = ctypes.c_char_p
+        L.moe_v41_strerror.argtypes = [i32]
+        for f in ("moe_v41_workspace_init", "moe_v41_quantize_q8_1", "moe_v41_select_from_logits", "moe_v41_route",
+                  "moe_v41_forward", "moe_v41_read_status"):
+            getattr(L, f).restype = i32
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().moe_v41_strerror(code).decode()
+
+
+def _p(t):
+    """device address of a tensor, or an int address, or None"""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, what)
+
+
+def make_cfg(dim, inter, n_routed, topk, gate_temp=1.0, norm_topk_prob=True, route_scale=1.5, swiglu_limit=10.0,
+             max_tokens=1, path=MOE_PATH_AUTO, wait_timeout_us=0) -> moe_v41_cfg:
+    return moe_v41_cfg(dim, inter, n_routed, topk, gate_temp, int(bool(norm_topk_prob)), route_scale, swiglu_limit,
+                       max_tokens, path, wait_timeout_us)
+
+
+def moe_v41_workspace_bytes(cfg: moe_v41_cfg) -> int:
+    return int(lib().moe_v41_workspace_bytes(ctypes.byref(cfg)))
+
+
+def moe_v41_workspace_init(ws, stream=None):
+    _check(lib().moe_v41_workspace_init(_p(ws), _nbytes(ws), _s(stream)), "moe_v41_workspace_init")
+
+
+def moe_v41_quantize_q8_1(x, x_is_f32: bool, rows: int, cols: int, q8_out, stream=None):
+    _check(lib().moe_v41_quantize_q8_1(_p(x), int(x_is_f32), rows, cols, _p(q8_out), _s(stream)),
+           "moe_v41_quantize_q8_1")
+
+
+def moe_v41_select_from_logits(cfg, logits, m, bias, topk_w, topk_idx, ws, stream=None):
+    _check(lib().moe_v41_select_from_logits(ctypes.byref(cfg), _p(logits), m, _p(bias), _p(topk_w), _p(topk_idx),
+                                            _p(ws), _nbytes(ws), _s(stream)), "moe_v41_select_from_logits")
+
+
+def moe_v41_route(cfg, x, m, router_w, bias, logits_out, topk_w, topk_idx, ws, stream=None):
+    _check(lib().moe_v41_route(ctypes.byref(cfg), _p(x), m, _p(router_w), _p(bias), _p(logits_out), _p(topk_w),
+                               _p(topk_idx), _p(ws), _nbytes(ws), _s(stream)), "moe_v41_route")
+
+
+def moe_v41_forward(cfg, x, m, router_w, bias, expert_ptrs, shared_kind, sh_w1, sh_w3, sh_w2, out, topk_w, topk_idx,
+                    logits_out, ws, stream=None):
+    _check(lib().moe_v41_forward(ctypes.byref(cfg), _p(x), m, _p(router_w), _p(bias), _p(expert_ptrs), shared_kind,
+                                 _p(sh_w1), _p(sh_w3), _p(sh_w2), _p(out), _p(topk_w), _p(topk_idx), _p(logits_out),
+                                 _p(ws), _nbytes(ws), _s(stream)), "moe_v41_forward")
+
+
+def moe_v41_read_status(ws, stream=None, clear: bool = False) -> int:
+    v = ctypes.c_uint32(0)
+    _check(lib().moe_v41_read_status(_p(ws), _s(stream), ctypes.byref(v), int(clear)), "moe_v41_read_status")
+    return v.value

@@ -1,0 +1,319 @@
+// Shared device code of the moe_v41 kernels (sm_103a): PTX wrappers for
+// mbarriers and 1-D bulk (TMA) copies, the workspace layout, the activation
+// "unit" layout the K-quant dot products read, and the Q2_K / Q3_K unit dots.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_v41.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- sizes
+constexpr int QK = 256;          // weights per K-quant super-block
+constexpr int Q2K_B = 84;        // bytes per Q2_K super-block
+constexpr int Q3K_B = 110;       // bytes per Q3_K super-block
+constexpr int Q8_B = 36;         // bytes per q8_1 block of 32
+constexpr int UNIT_WORDS = 24;   // words of one activation unit (see below)
+constexpr int MAX_TOPK = 16;
+constexpr int DECODE_MAX_M = 8;
+constexpr int MAXP = DECODE_MAX_M * MAX_TOPK;  // token/expert pairs of a decode call
+constexpr int MAX_N = 1024;
+
+// ------------------------------------------------- workspace control block
+struct Ctrl {
+  unsigned status;        // MOE_STATUS_* bits, sticky
+  unsigned route_arrive;  // last-block-done counter of the decode router
+  unsigned ticket_gu;     // work tickets of the decode gate/up kernel
+  unsigned ticket_dn;     // work tickets of the decode down kernel
+  unsigned pad[60];
+};
+
+// Routing of a decode call grouped by expert (ascending id), written by the
+// router's last block.
+struct DecodePlan {
+  int n_exp;                         // distinct experts picked
+  int n_pairs;                       // m * topk
+  int exp_id[MAXP];                  // ascending
+  int exp_off[MAXP + 1];             // pair range of each distinct expert
+  int pair_tok[MAXP];                // token of each pair, pairs sorted by (expert, token)
+  float pair_w[MAXP];                // routing weight G of each pair
+  unsigned long long exp_ptr[MAXP][3];  // w1, w3, w2 of each distinct expert (0 = skip)
+};
+
+// Byte offsets of the workspace regions (all 256-B aligned).
+struct WsLayout {
+  size_t ctrl, plan, logits, xq8, xu, hu, shh, total;
+};
+
+__host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Bytes of one activation vector of length K in unit layout.
+__host__ __device__ inline size_t unit_bytes(int K) { return (size_t)(K / QK) * 4 * UNIT_WORDS * 4; }
+
+inline WsLayout ws_layout(const moe_v41_cfg& c) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+  const size_t T = (size_t)c.max_tokens;
+  L.ctrl = take(sizeof(Ctrl));
+  L.plan = take(sizeof(DecodePlan));
+  L.logits = take(T * c.n_routed * sizeof(float));
+  L.xq8 = take(T * (c.dim / 32) * Q8_B);
+  L.xu = take(T * unit_bytes(c.dim));
+  const size_t pairs = (size_t)(T < DECODE_MAX_M ? T : DECODE_MAX_M) * c.topk;
+  L.hu = take(pairs * unit_bytes(c.inter));
+  const size_t shh_bf16 = (size_t)(T < DECODE_MAX_M ? T : DECODE_MAX_M) * c.inter * 2;
+  const size_t shh_q = (size_t)(T < DECODE_MAX_M ? T : DECODE_MAX_M) * unit_bytes(c.inter);
+  L.shh = take(shh_bf16 > shh_q ? shh_bf16 : shh_q);
+  L.total = off;
+  return L;
+}
+
+// Activation "unit" layout.  A vector of K values (K a multiple of 256) in
+// q8_1 blocks is stored per 256-block b and unit c (0..3) as 24 words:
+//   words 4j+w (j, w < 4): int8 x4 of elements 256b + 128(c>>1) + 32j + 16(c&1) + 4w .. +3
+//   word 16+j: f32 value of the fp16 d of q8_1 block 8b + 4(c>>1) + j
+//   word 20+j: int sum of the 16 quants of that half block
+// Unit c of a K-quant super-block holds exactly the 64 weights these 64
+// activations meet (quant bytes 16c..16c+15 of Q2_K, the four sub-blocks
+// 8(c>>1) + 2j + (c&1)), so one thread's dot needs one unit.
+
+// ------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// 1-D bulk copy global -> shared, completing on an mbarrier.  src, dst
+// 16-B aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and sets the timeout
+// status bit once) when the wait ran past the deadline.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t deadline,
+                                                  unsigned* status) {
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 63u) == 0 && globaltimer_ns() > deadline) {
+      atomicOr(status, (unsigned)MOE_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// dot of four unsigned bytes of a with four signed bytes of b, plus c
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t h16) {
+  return __half2float(__ushort_as_half((unsigned short)(h16 & 0xFFFFu)));
+}
+
+// Clipped SwiGLU in f32: g' = min(g, L), u' = clamp(u, -L, L) when L > 0;
+// h = g' sigmoid(g') u'.
+__device__ __forceinline__ float swiglu_f32(float g, float u, float L) {
+  if (L > 0.f) {
+    g = fminf(g, L);
+    u = fminf(fmaxf(u, -L), L);
+  }
+  float sig = 1.0f / (1.0f + expf(-g));
+  return g * sig * u;
+}
+
+// ------------------------------------------------------ K-quant unit dots
+// One activation unit in registers.
+struct XUnit {
+  int q[16];
+  float dq[4];
+  int s16[4];
+};
+
+__device__ __forceinline__ void load_xunit(XUnit& x, const int4* p) {
+  int4 v0 = __ldg(p + 0), v1 = __ldg(p + 1), v2 = __ldg(p + 2), v3 = __ldg(p + 3);
+  int4 v4 = __ldg(p + 4), v5 = __ldg(p + 5);
+  x.q[0] = v0.x; x.q[1] = v0.y; x.q[2] = v0.z; x.q[3] = v0.w;
+  x.q[4] = v1.x; x.q[5] = v1.y; x.q[6] = v1.z; x.q[7] = v1.w;
+  x.q[8] = v2.x; x.q[9] = v2.y; x.q[10] = v2.z; x.q[11] = v2.w;
+  x.q[12] = v3.x; x.q[13] = v3.y; x.q[14] = v3.z; x.q[15] = v3.w;
+  x.dq[0] = __int_as_float(v4.x); x.dq[1] = __int_as_float(v4.y);
+  x.dq[2] = __int_as_float(v4.z); x.dq[3] = __int_as_float(v4.w);
+  x.s16[0] = v5.x; x.s16[1] = v5.y; x.s16[2] = v5.z; x.s16[3] = v5.w;
+}
+
+// Unit c of a Q2_K block (84 B, 4-B aligned, in shared memory) dotted with
+// the matching activation unit:
+//   sum_j dq_j * ( d * sc_j * sum(q * qx) - dmin * m_j * sum(qx) )
+// over the four sub-blocks j of the unit.  The 2-bit plane j is masked in
+// place (values 4^j q), so its integer dot is shifted back by 2j.
+__device__ __forceinline__ float q2k_unit_dot(const uint8_t* blk, int c, const XUnit& x) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(blk);
+  const uint32_t q0 = w[4 + 4 * c], q1 = w[5 + 4 * c], q2 = w[6 + 4 * c], q3 = w[7 + 4 * c];
+  const int h = c >> 1, half = c & 1;
+  const uint32_t sa = w[2 * h], sb = w[2 * h + 1];
+  const uint32_t dd = w[20];
+  float acc_d = 0.f, acc_m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t mask = 0x03030303u << (2 * j);
+    int a = dp4a_us(q0 & mask, x.q[4 * j + 0], 0);
+    a = dp4a_us(q1 & mask, x.q[4 * j + 1], a);
+    a = dp4a_us(q2 & mask, x.q[4 * j + 2], a);
+    a = dp4a_us(q3 & mask, x.q[4 * j + 3], a);
+    const int isum = a >> (2 * j);
+    const uint32_t sw = (j < 2) ? sa : sb;
+    const uint32_t byte = (sw >> (8 * (half + 2 * (j & 1)))) & 0xFFu;
+    acc_d = fmaf(x.dq[j], (float)((int)(byte & 15u) * isum), acc_d);
+    acc_m = fmaf(x.dq[j], (float)((int)(byte >> 4) * x.s16[j]), acc_m);
+  }
+  const float d = half_bits_to_float(dd), dmin = half_bits_to_float(dd >> 16);
+  return d * acc_d - dmin * acc_m;
+}
+
+// 32-bit word at a 2-B aligned shared-memory address.
+__device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t* p) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uint32_t* base = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+  const uint32_t sh = (uint32_t)(a & 3u) * 8u;
+  return __funnelshift_r(base[0], base[1], sh);
+}
+
+// Unit c of a Q3_K block (110 B, 2-B aligned, in shared memory) dotted with
+// the matching activation unit.  q = lo + 4 hb - 4 with lo the 2-bit plane j
+// and hb bit 4h + j of the hmask byte:
+//   sum_j dq_j * d * (code_j - 32) * ( sum(lo*qx) + 4 sum(hb*qx) - 4 sum(qx) )
+__device__ __forceinline__ float q3k_unit_dot(const uint8_t* blk, int c, const XUnit& x) {
+  const int h = c >> 1, half = c & 1;
+  const uint8_t* qs = blk + 32 + 16 * c;
+  const uint8_t* hm = blk + 16 * half;
+  const uint32_t q0 = lds_u32_a2(qs), q1 = lds_u32_a2(qs + 4), q2 = lds_u32_a2(qs + 8), q3 = lds_u32_a2(qs + 12);
+  const uint32_t m0 = lds_u32_a2(hm), m1 = lds_u32_a2(hm + 4), m2 = lds_u32_a2(hm + 8), m3 = lds_u32_a2(hm + 12);
+  const uint32_t s_lo = lds_u32_a2(blk + 96);                        // scales bytes 0..3
+  const uint32_t s_lo2 = lds_u32_a2(blk + 100);                      // scales bytes 4..7
+  const uint32_t s_hi = lds_u32_a2(blk + 104);                       // scales bytes 8..11
+  const uint32_t dbits = (uint32_t)blk[108] | ((uint32_t)blk[109] << 8);
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lmask = 0x03030303u << (2 * j);
+    const uint32_t hmask = 0x01010101u << (4 * h + j);
+    int a = dp4a_us(q0 & lmask, x.q[4 * j + 0], 0);
+    a = dp4a_us(q1 & lmask, x.q[4 * j + 1], a);
+    a = dp4a_us(q2 & lmask, x.q[4 * j + 2], a);
+    a = dp4a_us(q3 & lmask, x.q[4 * j + 3], a);
+    int b = dp4a_us(m0 & hmask, x.q[4 * j + 0], 0);
+    b = dp4a_us(m1 & hmask, x.q[4 * j + 1], b);
+    b = dp4a_us(m2 & hmask, x.q[4 * j + 2], b);
+    b = dp4a_us(m3 & hmask, x.q[4 * j + 3], b);
+    const int isum = (a >> (2 * j)) + ((b >> (4 * h + j)) << 2) - 4 * x.s16[j];
+    // six-bit scale code of sub-block 8h + 2j + half
+    const int sbyte = 2 * j + half;  // 0..7
+    const uint32_t lo_src = sbyte < 4 ? s_lo : s_lo2;
+    const uint32_t lo4 = (lo_src >> (8 * (sbyte & 3) + 4 * h)) & 15u;
+    const uint32_t hi2 = (s_hi >> (8 * (2 * (j & 1) + half) + 2 * (2 * h + (j >> 1)))) & 3u;
+    const int scale = (int)(lo4 | (hi2 << 4)) - 32;
+    acc = fmaf(x.dq[j], (float)(scale * isum), acc);
+  }
+  return half_bits_to_float(dbits) * acc;
+}
+
+// ------------------------------------------------------------------ q8_1 (warp)
+// One warp quantises one q8_1 block of 32 values (lane i holds value i):
+// d = amax/127, q = round-half-away(v/d), decisions in f32.  Writes the
+// 36-byte block (if q8 != nullptr) and the block's two half units into the
+// unit layout of its vector (if units != nullptr).  qb = block index within
+// the vector.
+__device__ __forceinline__ void q8_block_warp(float v, int qb, uint8_t* q8, int* units) {
+  const int lane = threadIdx.x & 31;
+  float amax = fabsf(v);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const int q = amax == 0.0f ? 0 : (int)roundf(__fdiv_rn(v, d));
+  int s = q, s16;
+#pragma unroll
+  for (int o = 8; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);  // sums within 16-lane halves
+  s16 = s;
+  const int sum = s16 + __shfl_xor_sync(0xffffffffu, s16, 16);
+  // gather four bytes per word
+  uint32_t b = (uint32_t)(q & 0xFF);
+  uint32_t b1 = __shfl_down_sync(0xffffffffu, b, 1);
+  uint32_t b2 = __shfl_down_sync(0xffffffffu, b, 2);
+  uint32_t b3 = __shfl_down_sync(0xffffffffu, b, 3);
+  const uint32_t word = b | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  const __half d16 = __float2half_rn(d);
+  if (q8) {
+    uint8_t* blk = q8 + (size_t)qb * Q8_B;
+    if (lane == 0) {
+      const __half s16h = __float2half_rn(__fmul_rn(d, (float)sum));
+      const uint32_t hdr = (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(s16h) << 16);
+      *reinterpret_cast<uint32_t*>(blk) = hdr;
+    }
+    if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(blk + 4 + lane) = word;
+  }
+  if (units) {
+    const int b256 = qb >> 3, hj = qb & 7, h = hj >> 2, j = hj & 3;
+    const int half = lane >> 4;
+    int* u = units + ((size_t)b256 * 4 + 2 * h + half) * UNIT_WORDS;
+    if ((lane & 3) == 0) u[4 * j + ((lane & 15) >> 2)] = (int)word;
+    if ((lane & 15) == 0) {
+      u[16 + j] = __float_as_int(__half2float(d16));
+      u[20 + j] = s16;
+    }
+  }
+}
+
+}  // namespace moe

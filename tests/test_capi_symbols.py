@@ -1,0 +1,50 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, and exports
+every function include/*.h declares (no compute calls)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_v41_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import quantized_mixture_experts_router_gb300 as Q
+    import quantized_mixture_experts_router_gb300.build as qb
+    if not os.path.exists(Q.SO):
+        qb.build()
+    return ctypes.CDLL(Q.SO)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("moe_v41_route", "moe_v41_forward", "moe_v41_workspace_bytes", "moe_v41_read_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_workspace_sizing_is_host_only(lib):
+    import quantized_mixture_experts_router_gb300 as Q
+    cfg = Q.make_cfg(5120, 2304, 384, 6, max_tokens=8)
+    n = Q.moe_v41_workspace_bytes(cfg)
+    assert n > 0 and n % 256 == 0
+    assert Q.moe_v41_workspace_bytes(Q.make_cfg(5000, 2304, 384, 6)) == 0      # dim not a multiple of 256
+    assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 17)) == 0     # topk above 16
+    assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 4, 6)) == 0        # topk above n_routed
+    assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, gate_temp=0.0)) == 0
+    assert Q.strerror(Q.MOE_ERR_WORKSPACE).startswith("workspace")
