@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Benchmark of the moe_v41 hot path on GB300.
+
+Default workload: the full-shape decode step, 40 independent MoE layers
+(dim 5120, inter 2304, 384 routed experts, top-6, m = 1, bf16 shared expert),
+every routed expert resident in HBM behind a slot-pointer table.  One step is
+one pass of all 40 layers for one token: router + selection on the device,
+q8_1(x), Q2_K gate/up + clipped SwiGLU + q8_1(h), Q3_K down, G-weighted sum,
+shared expert added last.
+
+Prints one JSON line (rank 0).  `value` is tokens/s through the 40-layer step
+with inputs resident in HBM; `e2e` is the same metric through the C-ABI with
+host buffers copied in and out inside the timed region.  `--impl reference`
+times the CPU oracle instead (the reference arm of this benchmark).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth.workloads as W  # noqa: E402
+
+HBM_FALLBACK_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_m1_40layer", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0, help="layers per step (default: the workload's)")
+    ap.add_argument("--resident-layers", type=int, default=0,
+                    help="distinct layer weight sets held on the device (default: all layers)")
+    ap.add_argument("--resident-experts", type=int, default=0,
+                    help="expert slots held per layer (default: all; fewer alias experts, for small profiling runs)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ utils
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def algorithmic_bytes(w: W.Workload, distinct: float) -> float:
+    """Bytes the method must move for one layer call: router weight and bias,
+    the distinct routed experts' blocks, the shared expert, x in, out out."""
+    router = w.n_routed * w.dim * 2 + w.n_routed * 4
+    shared = 3 * w.dim * w.inter * 2 if w.shared_kind == W.SHARED_BF16 else w.expert_bytes
+    return router + distinct * w.expert_bytes + shared + w.m * w.dim * 2 + w.m * w.dim * 4
+
+
+def sources_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_mixture_experts_router_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per layer call from the committed ncu summary, if it was
+    taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("sources_sha256_16") != sources_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_layer_call"])
+    except (KeyError, ValueError):
+        return None
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------- oracle (CPU)
+
+def _oracle_inputs(w: W.Workload, layer: int):
+    import oracle
+    x, R, b, sh = W.x_bf16(w, layer), W.router_bf16(w, layer), W.bias_f32(w, layer), W.shared_weights(w, layer)
+    z = oracle.router_logits(x, R)
+    _, idx, _ = oracle.route_from_logits(oracle.cfg_of(w), z, b)
+    experts = [None] * w.n_routed
+    for e in np.unique(idx):
+        experts[int(e)] = W.expert_blocks(w, layer, int(e))
+    return x, R, b, experts, sh
+
+
+def _oracle_run(w: W.Workload, inp, token: int):
+    import oracle
+    x, R, b, experts, sh = inp
+    oracle.moe_layer(oracle.cfg_of(w), x, R, b, experts, w.shared_kind, *sh, tokens=[token], nthreads=1)
+
+
+def cpu_baseline(w: W.Workload, layers_per_step: int, n_units: int, threads: int):
+    """Time the oracle on n_units (layer, token) units spread over `threads`
+    host threads.  Returns (tokens/s, seconds, description)."""
+    units = [(u % w.layers if w.layers > 1 else 0, (u // max(1, w.layers)) % w.m) for u in range(n_units)]
+    layers = sorted(set(l for l, _ in units))
+    with ThreadPoolExecutor(min(threads, 8)) as ex:
+        inputs = dict(zip(layers, ex.map(lambda l: _oracle_inputs(w, l), layers)))
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda u: _oracle_run(w, inputs[u[0]], u[1]), units))
+    dt = time.perf_counter() - t0
+    # one step = layers_per_step layer calls of m tokens: tokens/s = units / (layers_per_step) / dt
+    tps = n_units / layers_per_step / dt
+    desc = f"{n_units} (layer, token) units of {w.name} ({len(layers)} layers) on {threads} threads"
+    return tps, dt, desc
+
+
+# ------------------------------------------------------------------- GPU
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import quantized_mixture_experts_router_gb300 as Q
+    from synth.device import stage_layer
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = W.WORKLOADS[args.workload]
+    L = args.layers or w.layers
+    free, total = torch.cuda.mem_get_info()
+    per_layer = w.n_routed * (w.expert_bytes + 1024) + 3 * w.dim * w.inter * 2 + w.n_routed * w.dim * 2
+    resident = args.resident_layers or L
+    fit = max(1, int((free - (8 << 30)) // per_layer))
+    rotated = resident > fit
+    resident = min(resident, fit)
+    layers = [stage_layer(w, l, device=dev, experts_on_gpu=True, bulk_on_gpu=True, slots=args.resident_experts)
+              for l in range(resident)]
+    # x of every layer of the step (the layer's own seeded rows)
+    xs = [layers[l % resident].x if l < resident else stage_x(w, l, dev) for l in range(L)]
+    cfg = Q.make_cfg(w.dim, w.inter, w.n_routed, w.topk, w.gate_temp, w.norm_topk_prob, w.route_scale,
+                     w.swiglu_limit, max_tokens=w.m)
+    ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    Q.moe_v41_workspace_init(ws)
+    out = torch.empty((L, w.m, w.dim), dtype=torch.float32, device=dev)
+    tw = torch.empty((L, w.m, w.topk), dtype=torch.float32, device=dev)
+    ti = torch.empty((L, w.m, w.topk), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def layer_call(l, x=None):
+        d = layers[l % resident]
+        Q.moe_v41_forward(cfg, xs[l] if x is None else x, w.m, d.router_w, d.bias, d.expert_ptrs, w.shared_kind,
+                          d.sh1, d.sh3, d.sh2, out[l], tw[l], ti[l], None, ws, stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        for l in range(L):
+            layer_call(l)
+    st = Q.moe_v41_read_status(ws, stream, clear=True)
+    if st:
+        raise RuntimeError(f"device status {st} during warm-up")
+    distinct = float(np.mean([np.unique(ti[l].cpu().numpy()).size for l in range(L)]))
+
+    # --- device-resident timed region, one event per layer boundary
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(K)]
+    barrier()
+    clocks = Clocks(local_rank)
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(K):
+        for l in range(L):
+            evs[k][l].record(stream)
+            layer_call(l)
+        evs[k][L].record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    per_call_ms = statistics.fmean(evs[k][l].elapsed_time(evs[k][l + 1]) for k in range(K) for l in range(L))
+    st = Q.moe_v41_read_status(ws, stream, clear=True)
+    if st:
+        raise RuntimeError(f"device status {st} during the timed region")
+
+    # --- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = [torch.empty((w.m, w.dim), dtype=torch.int16).pin_memory() for _ in range(L)]
+        for l in range(L):
+            xh[l].copy_(xs[l].cpu())
+        oh = torch.empty((L, w.m, w.dim), dtype=torch.float32).pin_memory()
+        xd = torch.empty((L, w.m, w.dim), dtype=torch.int16, device=dev)
+        Ke = max(1, K // 2)
+        for _ in range(2):
+            for l in range(L):
+                xd[l].copy_(xh[l], non_blocking=True)
+                layer_call(l, xd[l])
+                oh[l].copy_(out[l], non_blocking=True)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            for l in range(L):
+                xd[l].copy_(xh[l], non_blocking=True)
+                layer_call(l, xd[l])
+                oh[l].copy_(out[l], non_blocking=True)
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        e2e = dict(ms=e_ms, steps=Ke, h2d=L * w.m * w.dim * 2, d2h=L * w.m * w.dim * 4)
+
+    # max over ranks
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e["ms"] if e2e else 0.0], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+        if e2e:
+            e2e["ms"] = float(t[1])
+    return dict(w=w, L=L, K=K, ms=ms, per_call_ms=per_call_ms, distinct=distinct, clocks=clk, e2e=e2e,
+                resident=resident, rotated=rotated, launches_per_call=3 if w.m <= 8 else None,
+                resident_experts=args.resident_experts)
+
+
+def stage_x(w, l, dev):
+    import torch
+    from synth.device import x_gpu
+    t = torch.empty((w.m, w.dim), dtype=torch.int16, device=dev)
+    x_gpu(w, l, t)
+    return t
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = W.WORKLOADS[args.workload]
+    L = args.layers or w.layers
+    ncores = os.cpu_count() or 1
+
+    if args.impl == "reference":
+        # the CPU oracle as the reference arm: rank 0 only
+        if rank != 0:
+            return
+        K, Wm = args.steps, args.warmup
+        cpu_baseline(w, L, max(1, min(Wm, ncores)), ncores)  # warm-up units
+        tps, dt, desc = cpu_baseline(w, L, K, ncores)
+        line = {"impl": "reference", "metric": metric_name(w), "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": K, "warmup": Wm, "ms_per_step": dt * 1000.0 / K * ncores, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config_of(w, L, None),
+                "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
+                                 "sample": f"each step one (layer, token) unit; {desc}"},
+                "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = run_ours(args, rank, world, local_rank)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    K = r["K"]
+    sec = r["ms"] / 1000.0
+    tokens = world * w.m * K  # each step moves m tokens through all L layers, per GPU
+    value = tokens / sec
+    hbm, kind = peaks()
+    bytes_call = algorithmic_bytes(w, r["distinct"])
+    achieved = bytes_call / (r["per_call_ms"] / 1000.0) / 1e9
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": metric_name(w), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": r["ms"] / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8-dp4a/bf16-fma, f32 accumulate", "data": "synthetic",
+        "config": config_of(w, L, r),
+        "roofline": {"bound": "hbm", "kernel": "moe_v41_forward (3 launches: route, gate/up, down)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_kind": kind, "traffic": traffic, "algorithmic_bytes_per_call": bytes_call,
+                     "us_per_call": r["per_call_ms"] * 1000.0, "frac_of_8tbs": achieved / 8000.0},
+        "gpu_launches": (r["launches_per_call"] or 0) * L * K,
+        "clocks": r["clocks"],
+    }
+    if r["e2e"]:
+        e = r["e2e"]
+        line["e2e"] = {"value": world * w.m * e["steps"] / (e["ms"] / 1000.0), "unit": "tokens/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    if world == 1 and not args.no_cpu_baseline:
+        n_units = min(ncores, L * w.m)
+        tps, dt, desc = cpu_baseline(w, L, n_units, ncores)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
+                                "sample": desc + f", {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def metric_name(w: W.Workload) -> str:
+    return f"MoE-layer tokens/s, {w.name} (m={w.m}, {w.layers} layer(s) per step)"
+
+
+def config_of(w: W.Workload, L: int, r):
+    c = {"workload": w.name, "dim": w.dim, "inter": w.inter, "n_routed": w.n_routed, "topk": w.topk, "m": w.m,
+         "layers_per_step": L, "shared": "bf16" if w.shared_kind == W.SHARED_BF16 else "Q2_K/Q3_K",
+         "experts": "Q2_K gate/up, Q3_K down, all resident in HBM",
+         "l2": "inputs larger than L2: each step streams every layer's weights (>6 GB) through the 129 MB L2"}
+    if r:
+        c["distinct_experts_per_call"] = r["distinct"]
+        c["resident_layers"] = r["resident"]
+        if r.get("resident_experts"):
+            c["resident_experts"] = r["resident_experts"]
+            c["note_experts"] = "profiling run: expert e uses slot e % resident_experts"
+        if r["rotated"]:
+            c["note"] = "device memory held fewer layers than the step; layers rotate over the resident ones"
+    return c
+
+
+if __name__ == "__main__":
+    main()

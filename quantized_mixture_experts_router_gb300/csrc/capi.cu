@@ -57,8 +57,6 @@ RouteParams route_params(const moe_v41_cfg* c, const void* x, int m, const void*
   p.topk_w = topk_w; p.topk_idx = topk_idx;
   p.xq8 = ws + L.xq8;
   p.xu = reinterpret_cast<int*>(ws + L.xu);
-  p.plan = reinterpret_cast<DecodePlan*>(ws + L.plan);
-  p.expert_ptrs = nullptr;
   p.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
   return p;
 }
@@ -75,7 +73,7 @@ size_t moe_v41_workspace_bytes(const moe_v41_cfg* cfg) {
 int moe_v41_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
   if (!aligned(ws, 256)) return MOE_ERR_ALIGN;
-  return cudaMemsetAsync(ws, 0, sizeof(Ctrl), (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int moe_v41_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols, void* q8_out, void* stream) {
@@ -110,7 +108,6 @@ int moe_v41_route(const moe_v41_cfg* cfg, const void* x, int m, const void* rout
   uint8_t* w = static_cast<uint8_t*>(ws);
   if (m <= DECODE_MAX_M && cfg->path != MOE_PATH_PREFILL) {
     RouteParams p = route_params(cfg, x, m, router_w, bias, logits_out, topk_w, topk_idx, w, L);
-    p.plan = nullptr;
     return launch_route_decode(p, (cudaStream_t)stream);
   }
   return MOE_ERR_ARG;  // the prefill router is added with the prefill path
@@ -137,26 +134,37 @@ int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const void* ro
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
 
-  RouteParams rp = route_params(cfg, x, m, router_w, bias, logits_out, topk_w, topk_idx, w, L);
-  rp.expert_ptrs = reinterpret_cast<const unsigned long long*>(expert_ptrs);
-  if ((rc = launch_route_decode(rp, s))) return rc;
-
+  if (!decode_fits(cfg->dim, cfg->inter)) return MOE_ERR_ARG;
   DecodeParams dp{};
-  dp.m = m; dp.D = cfg->dim; dp.I = cfg->inter; dp.k = cfg->topk;
-  dp.swiglu_limit = cfg->swiglu_limit;
+  dp.m = m; dp.D = cfg->dim; dp.I = cfg->inter; dp.N = cfg->n_routed; dp.k = cfg->topk;
+  dp.norm = cfg->norm_topk_prob != 0;
+  dp.gate_temp = cfg->gate_temp; dp.route_scale = cfg->route_scale; dp.swiglu_limit = cfg->swiglu_limit;
   dp.shared_kind = shared_kind;
+  dp.x = static_cast<const uint16_t*>(x);
+  dp.router_w = static_cast<const uint16_t*>(router_w);
+  dp.bias = bias;
+  dp.expert_ptrs = reinterpret_cast<const unsigned long long*>(expert_ptrs);
   dp.sh1 = static_cast<const uint8_t*>(sh_w1);
   dp.sh3 = static_cast<const uint8_t*>(sh_w3);
   dp.sh2 = static_cast<const uint8_t*>(sh_w2);
-  dp.x = static_cast<const uint16_t*>(x);
-  dp.xu = reinterpret_cast<const int*>(w + L.xu);
+  dp.logits = logits_out ? logits_out : reinterpret_cast<float*>(w + L.logits);
+  dp.topk_w = topk_w; dp.topk_idx = topk_idx;
+  dp.xq8 = w + L.xq8;
+  dp.xu = reinterpret_cast<int*>(w + L.xu);
+  dp.hf = reinterpret_cast<float*>(w + L.hf);
   dp.hu = reinterpret_cast<int*>(w + L.hu);
+  dp.shgu = reinterpret_cast<float*>(w + L.shgu);
   dp.shh = w + L.shh;
-  dp.plan = reinterpret_cast<const DecodePlan*>(w + L.plan);
+  dp.ep = reinterpret_cast<float*>(w + L.ep);
+  dp.sp = reinterpret_cast<float*>(w + L.sp);
+  dp.cnt = reinterpret_cast<unsigned*>(w + L.cnt);
+  dp.plan_w = reinterpret_cast<DecodePlan*>(w + L.plan);
+  const int Td = cfg->max_tokens < DECODE_MAX_M ? cfg->max_tokens : DECODE_MAX_M;
+  dp.shvec0 = Td * cfg->topk;
   dp.out = out;
   dp.ctrl = reinterpret_cast<Ctrl*>(w + L.ctrl);
   dp.timeout_ns = timeout_ns(cfg);
-  return launch_decode_experts(dp, sms, s);
+  return launch_decode_layer(dp, sms, s);
 }
 
 int moe_v41_read_status(void* ws, void* stream, uint32_t* status, int clear) {

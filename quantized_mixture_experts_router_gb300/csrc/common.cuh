@@ -26,14 +26,19 @@ constexpr int MAX_N = 1024;
 // ------------------------------------------------- workspace control block
 struct Ctrl {
   unsigned status;        // MOE_STATUS_* bits, sticky
-  unsigned route_arrive;  // last-block-done counter of the decode router
-  unsigned ticket_gu;     // work tickets of the decode gate/up kernel
-  unsigned ticket_dn;     // work tickets of the decode down kernel
-  unsigned pad[60];
+  unsigned route_arrive;  // last-block-done counter of the standalone router
+  unsigned ticket;        // work tickets of the fused decode kernel
+  unsigned q8_done;       // q8_1(x) tasks finished
+  unsigned router_done;   // router tasks finished
+  unsigned route_ready;   // the decode plan is written
+  unsigned shgu_done;     // shared-expert gate/up tasks finished
+  unsigned rtgu_done;     // routed gate/up tasks finished
+  unsigned exit_count;    // blocks that have left the fused kernel
+  unsigned pad[55];
 };
 
 // Routing of a decode call grouped by expert (ascending id), written by the
-// router's last block.
+// warp that finishes the last router task.
 struct DecodePlan {
   int n_exp;                         // distinct experts picked
   int n_pairs;                       // m * topk
@@ -41,12 +46,14 @@ struct DecodePlan {
   int exp_off[MAXP + 1];             // pair range of each distinct expert
   int pair_tok[MAXP];                // token of each pair, pairs sorted by (expert, token)
   float pair_w[MAXP];                // routing weight G of each pair
-  unsigned long long exp_ptr[MAXP][3];  // w1, w3, w2 of each distinct expert (0 = skip)
+  int tok_pairs[DECODE_MAX_M][MAX_TOPK];  // each token's pairs in ascending expert id
+  unsigned long long exp_ptr[MAXP][3];    // w1, w3, w2 of each distinct expert (0 = skip)
 };
 
 // Byte offsets of the workspace regions (all 256-B aligned).
 struct WsLayout {
-  size_t ctrl, plan, logits, xq8, xu, hu, shh, total;
+  size_t ctrl, plan, cnt, logits, xq8, xu, hf, hu, shgu, shh, ep, sp, total;
+  size_t cnt_words;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -54,21 +61,34 @@ __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_
 // Bytes of one activation vector of length K in unit layout.
 __host__ __device__ inline size_t unit_bytes(int K) { return (size_t)(K / QK) * 4 * UNIT_WORDS * 4; }
 
+// Counter arrays of the fused decode kernel (words): the shared expert's
+// per-row gate/up pairing, the per-(vector, 32-row) q8_1(h) groups and the
+// per-8-row output groups.
+__host__ __device__ inline int cnt_shpair(int) { return 0; }
+__host__ __device__ inline int cnt_hgrp(int I) { return I; }
+__host__ __device__ inline int cnt_dgrp(int I) { return I + (MAXP + DECODE_MAX_M) * (I / 32); }
+__host__ __device__ inline int cnt_words(int D, int I) { return cnt_dgrp(I) + D / 8; }
+
 inline WsLayout ws_layout(const moe_v41_cfg& c) {
   WsLayout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
   const size_t T = (size_t)c.max_tokens;
+  const size_t Td = T < DECODE_MAX_M ? T : DECODE_MAX_M;
+  const size_t vecs = Td * c.topk + Td;  // routed pairs, then the shared expert's tokens
   L.ctrl = take(sizeof(Ctrl));
   L.plan = take(sizeof(DecodePlan));
+  L.cnt_words = (size_t)cnt_words(c.dim, c.inter);
+  L.cnt = take(L.cnt_words * 4);
   L.logits = take(T * c.n_routed * sizeof(float));
   L.xq8 = take(T * (c.dim / 32) * Q8_B);
   L.xu = take(T * unit_bytes(c.dim));
-  const size_t pairs = (size_t)(T < DECODE_MAX_M ? T : DECODE_MAX_M) * c.topk;
-  L.hu = take(pairs * unit_bytes(c.inter));
-  const size_t shh_bf16 = (size_t)(T < DECODE_MAX_M ? T : DECODE_MAX_M) * c.inter * 2;
-  const size_t shh_q = (size_t)(T < DECODE_MAX_M ? T : DECODE_MAX_M) * unit_bytes(c.inter);
-  L.shh = take(shh_bf16 > shh_q ? shh_bf16 : shh_q);
+  L.hf = take(vecs * c.inter * sizeof(float));
+  L.hu = take(vecs * unit_bytes(c.inter));
+  L.shgu = take(Td * 2 * c.inter * sizeof(float));
+  L.shh = take(Td * c.inter * 2);
+  L.ep = take(Td * c.topk * c.dim * sizeof(float));
+  L.sp = take(Td * c.dim * sizeof(float));
   L.total = off;
   return L;
 }

@@ -27,24 +27,35 @@ struct RouteParams {
   int* topk_idx;
   uint8_t* xq8;              // q8_1 blocks [m][D/32]
   int* xu;                   // unit layout [m][...]
-  DecodePlan* plan;          // nullptr: routing only
-  const unsigned long long* expert_ptrs;
   Ctrl* ctrl;
 };
 
 struct DecodeParams {
-  int m, D, I, k;
-  float swiglu_limit;
+  int m, D, I, N, k, norm;
+  float gate_temp, route_scale, swiglu_limit;
   int shared_kind;
+  const uint16_t* x;         // bf16 [m, D]
+  const uint16_t* router_w;  // bf16 [N, D]
+  const float* bias;         // [N]
+  const unsigned long long* expert_ptrs;  // [N][3]
   const uint8_t* sh1;
   const uint8_t* sh3;
   const uint8_t* sh2;
-  const uint16_t* x;     // bf16 [m, D]
-  const int* xu;         // unit layout of q8_1(x)
-  int* hu;               // unit layout of q8_1(h), one vector per pair
-  uint8_t* shh;          // shared h: bf16 [m, I] or unit layout per token
-  const DecodePlan* plan;
-  float* out;            // f32 [m, D]
+  float* logits;             // [m, N]
+  float* topk_w;             // [m, k]
+  int* topk_idx;             // [m, k]
+  uint8_t* xq8;              // q8_1 blocks of x
+  int* xu;                   // unit layout of q8_1(x)
+  float* hf;                 // h in f32, one row of I per vector (pairs, then shared tokens)
+  int* hu;                   // unit layout of q8_1(h), one per vector
+  float* shgu;               // bf16 shared expert: g and u per token
+  uint8_t* shh;              // bf16 shared expert: h [m, I] bf16
+  float* ep;                 // E of each pair [pairs, D]
+  float* sp;                 // shared expert output [m, D]
+  unsigned* cnt;             // counter arrays
+  DecodePlan* plan_w;
+  int shvec0;                // first vector index of the shared expert's tokens
+  float* out;                // f32 [m, D]
   Ctrl* ctrl;
   unsigned long long timeout_ns;
 };
@@ -52,6 +63,8 @@ struct DecodeParams {
 int launch_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols, void* q8, cudaStream_t s);
 int launch_select(const SelectParams& p, cudaStream_t s);
 int launch_route_decode(const RouteParams& p, cudaStream_t s);
-int launch_decode_experts(const DecodeParams& p, int num_sms, cudaStream_t s);
+int launch_decode_layer(const DecodeParams& p, int num_sms, cudaStream_t s);
+bool decode_fits(int D, int I);
+size_t decode_smem_bytes();
 
 }  // namespace moe

@@ -65,6 +65,9 @@ def gpu_lib():
         lib.syn_gpu_fill_q3k.argtypes = [vp, u64, u64, u64, dbl, dbl, vp]
         lib.syn_gpu_fill_normal_bf16.argtypes = [vp, u64, u64, u64, dbl, vp, vp]
         lib.syn_gpu_fill_uniform_f32.argtypes = [vp, u64, u64, dbl, dbl, vp]
+        lib.syn_gpu_fill_experts.argtypes = [vp, ctypes.c_uint32, u64, u64, u64, u64, u64, u64, u64,
+                                             ctypes.c_uint32, vp]
+        lib.syn_gpu_fill_experts.restype = ctypes.c_int
         for f in ("syn_gpu_fill_q2k", "syn_gpu_fill_q3k", "syn_gpu_fill_normal_bf16", "syn_gpu_fill_uniform_f32"):
             getattr(lib, f).restype = ctypes.c_int
         _gpu = lib

@@ -57,18 +57,12 @@ def _check(rc, what):
 
 
 def fill_experts_gpu(w: Workload, layer: int, buf: torch.Tensor) -> None:
-    """Draw all routed experts of a layer into buf [n_routed, slot] on the GPU."""
-    g = gpu_lib()
+    """Draw the routed experts 0..buf.shape[0]-1 of a layer into buf [slots, slot] on the GPU."""
     o1, o3, o2, slot = slot_layout(w)
     nb1 = w.inter * (w.dim // 256)
     nb2 = w.dim * (w.inter // 256)
-    base = buf.data_ptr()
-    s = _stream()
-    for e in range(w.n_routed):
-        p = base + e * slot
-        _check(g.syn_gpu_fill_q2k(p + o1, nb1, 0, key(w.seed, layer, T_W1, e), 1e-3, 4e-3, s), "fill w1")
-        _check(g.syn_gpu_fill_q2k(p + o3, nb1, 0, key(w.seed, layer, T_W3, e), 1e-3, 4e-3, s), "fill w3")
-        _check(g.syn_gpu_fill_q3k(p + o2, nb2, 0, key(w.seed, layer, T_W2, e), 5e-4, 2e-3, s), "fill w2")
+    _check(gpu_lib().syn_gpu_fill_experts(buf.data_ptr(), buf.shape[0], slot, o1, o3, o2, nb1, nb2, w.seed, layer,
+                                          _stream()), "fill experts")
 
 
 def fill_experts_host(w: Workload, layer: int, buf: torch.Tensor, experts=None) -> None:
@@ -87,13 +81,17 @@ def fill_experts_host(w: Workload, layer: int, buf: torch.Tensor, experts=None) 
 
 
 def pointer_table(w: Workload, buf: torch.Tensor) -> torch.Tensor:
+    """[n_routed, 3] device addresses; with fewer slots than experts, expert e
+    uses slot e % slots (a profiling aid: same bytes per call, fewer held)."""
     o1, o3, o2, slot = slot_layout(w)
     base = buf.data_ptr()
+    slots = buf.shape[0]
     t = torch.empty((w.n_routed, 3), dtype=torch.int64)
     for e in range(w.n_routed):
-        t[e, 0] = base + e * slot + o1
-        t[e, 1] = base + e * slot + o3
-        t[e, 2] = base + e * slot + o2
+        s = e % slots
+        t[e, 0] = base + s * slot + o1
+        t[e, 1] = base + s * slot + o3
+        t[e, 2] = base + s * slot + o2
     return t.to(buf.device)
 
 
@@ -109,19 +107,22 @@ def fill_normal_bf16_gpu(t: torch.Tensor, k: int, std: float, cols: int, rs: tor
 
 
 def stage_layer(w: Workload, layer: int, device="cuda", experts_on_gpu: bool = True,
-                bulk_on_gpu: bool = False) -> DeviceLayer:
+                bulk_on_gpu: bool = False, slots: int = 0) -> DeviceLayer:
     """All of one layer's inputs on the device.
 
     experts_on_gpu: draw the routed experts with the GPU twin (else host).
     bulk_on_gpu: also draw the bf16 shared expert and the router on the GPU
     (fast; bytes can differ from the host draw in rare last-ulp cases, so
     parity tests keep it off).
+    slots: expert slots held (default n_routed); fewer slots alias experts.
     """
     o1, o3, o2, slot = slot_layout(w)
-    experts = torch.empty((w.n_routed, slot), dtype=torch.uint8, device=device)
+    slots = slots or w.n_routed
+    experts = torch.empty((slots, slot), dtype=torch.uint8, device=device)
     if experts_on_gpu:
         fill_experts_gpu(w, layer, experts)
     else:
+        assert slots == w.n_routed
         fill_experts_host(w, layer, experts)
     ptrs = pointer_table(w, experts)
     x = _bits_to_dev(x_bf16(w, layer), device)
