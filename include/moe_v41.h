@@ -137,6 +137,38 @@ MOE_API int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const 
                     const void* sh_w2, float* out, float* topk_w, int32_t* topk_idx, float* logits_out, void* ws,
                     size_t ws_bytes, void* stream);
 
+/* Bytes of the fixed scratch array behind moe_v41_forward_noalloc (4 MiB).
+ * Each GPU that loads this library holds it until the process exits. */
+#define MOE_V41_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* moe_v41_forward for up to eight tokens (the decode kernels) WITHOUT a
+ * caller workspace: the scratch lives in a fixed 4 MiB array owned by the
+ * library on each device.  The pages describe no such call; it exists for
+ * callers that have no way to obtain device memory at call time: a plugin
+ * running inside a host engine that owns every byte of the GPU's memory
+ * through its own pool and hands plugins no allocator, or a latency-critical
+ * loop that must not call cudaMalloc (which can synchronise the device).
+ *   Arguments are those of moe_v41_forward minus ws/ws_bytes, plus
+ *   status_out: a DEVICE uint32_t (may be NULL) that receives this call's
+ *   MOE_STATUS_* bits, written asynchronously on `stream`.
+ *   Limits: cfg->max_tokens <= 8 and 1 <= m <= cfg->max_tokens; the
+ *   workspace moe_v41_workspace_bytes(cfg) would need must fit in
+ *   MOE_V41_NOALLOC_SCRATCH_BYTES, else MOE_ERR_WORKSPACE (the DeepSeek-V4.1
+ *   shape, dim 5120 / inter 2304 / 384 experts / top-6 at 8 tokens, needs about
+ *   2.3 MB).  Nothing is allocated: no cudaMalloc, cudaFree or allocating
+ *   library call.
+ *   Set-up: the first call on a device (with that device current) looks up
+ *   the array's device address once; make that first call before any stream
+ *   capture.  Each call first clears the control words and counters it
+ *   starts from.  All calls share the one array, so calls whose work overlaps
+ *   on the GPU (different streams, or different host threads) race: serialise
+ *   them, e.g. by issuing them on one stream. */
+MOE_API int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w,
+                                    const float* bias, const uint64_t* expert_ptrs, int shared_kind,
+                                    const void* sh_w1, const void* sh_w3, const void* sh_w2, float* out,
+                                    float* topk_w, int32_t* topk_idx, float* logits_out, uint32_t* status_out,
+                                    void* stream);
+
 /* Synchronise `stream`, then copy the workspace status word (MOE_STATUS_* bits
  * accumulated since the last clear) to *status (host memory); clear == non-zero
  * resets it to 0. */

@@ -50,10 +50,11 @@ def lib():
         L.moe_v41_route.argtypes = [cfgp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.moe_v41_forward.argtypes = [cfgp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.moe_v41_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32), i32]
+        L.moe_v41_forward_noalloc.argtypes = [cfgp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_v41_strerror.restype = ctypes.c_char_p
         L.moe_v41_strerror.argtypes = [i32]
         for f in ("moe_v41_workspace_init", "moe_v41_quantize_q8_1", "moe_v41_select_from_logits", "moe_v41_route",
-                  "moe_v41_forward", "moe_v41_read_status"):
+                  "moe_v41_forward", "moe_v41_read_status", "moe_v41_forward_noalloc"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -124,6 +125,20 @@ def moe_v41_forward(cfg, x, m, router_w, bias, expert_ptrs, shared_kind, sh_w1, 
     _check(lib().moe_v41_forward(ctypes.byref(cfg), _p(x), m, _p(router_w), _p(bias), _p(expert_ptrs), shared_kind,
                                  _p(sh_w1), _p(sh_w3), _p(sh_w2), _p(out), _p(topk_w), _p(topk_idx), _p(logits_out),
                                  _p(ws), _nbytes(ws), _s(stream)), "moe_v41_forward")
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def moe_v41_forward_noalloc(cfg, x, m, router_w, bias, expert_ptrs, shared_kind, sh_w1, sh_w3, sh_w2, out, topk_w,
+                            topk_idx, logits_out=None, status_out=None, stream=None):
+    """moe_v41_forward without a workspace: the library's own fixed scratch
+    array (4 MiB per device) is used.  For callers that cannot allocate device
+    memory when they call; see include/moe_v41.h for the limits."""
+    _check(lib().moe_v41_forward_noalloc(ctypes.byref(cfg), _p(x), m, _p(router_w), _p(bias), _p(expert_ptrs),
+                                         shared_kind, _p(sh_w1), _p(sh_w3), _p(sh_w2), _p(out), _p(topk_w),
+                                         _p(topk_idx), _p(logits_out), _p(status_out), _s(stream)),
+           "moe_v41_forward_noalloc")
 
 
 def moe_v41_read_status(ws, stream=None, clear: bool = False) -> int:
