@@ -285,7 +285,8 @@ def run_ours(args, rank, world, local_rank):
         if e2e:
             e2e["ms"] = float(t[1])
     return dict(w=w, L=L, K=K, ms=ms, per_call_ms=per_call_ms, distinct=distinct, clocks=clk, e2e=e2e,
-                resident=resident, rotated=rotated, launches_per_call=3 if w.m <= 8 else None,
+                resident=resident, rotated=rotated, launches_per_call=1 if w.m <= 8 else None,
+                kernel="k_decode_layer (the whole layer call, one launch)" if w.m <= 8 else "prefill kernels",
                 resident_experts=args.resident_experts)
 
 
@@ -345,7 +346,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": r["ms"] / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8-dp4a/bf16-fma, f32 accumulate", "data": "synthetic",
         "config": config_of(w, L, r),
-        "roofline": {"bound": "hbm", "kernel": "moe_v41_forward (3 launches: route, gate/up, down)",
+        "roofline": {"bound": "hbm", "kernel": r["kernel"],
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_kind": kind, "traffic": traffic, "algorithmic_bytes_per_call": bytes_call,
                      "us_per_call": r["per_call_ms"] * 1000.0, "frac_of_8tbs": achieved / 8000.0},

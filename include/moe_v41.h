@@ -137,12 +137,12 @@ MOE_API int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const 
                     const void* sh_w2, float* out, float* topk_w, int32_t* topk_idx, float* logits_out, void* ws,
                     size_t ws_bytes, void* stream);
 
-/* Bytes of the fixed scratch array behind moe_v41_forward_noalloc (4 MiB).
+/* Bytes of the fixed scratch array behind moe_v41_forward_noalloc (512 KiB).
  * Each GPU that loads this library holds it until the process exits. */
-#define MOE_V41_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define MOE_V41_NOALLOC_SCRATCH_BYTES (512u << 10)
 
 /* moe_v41_forward for up to eight tokens (the decode kernels) WITHOUT a
- * caller workspace: the scratch lives in a fixed 4 MiB array owned by the
+ * caller workspace: the scratch lives in a fixed 512 KiB array owned by the
  * library on each device.  The pages describe no such call; it exists for
  * callers that have no way to obtain device memory at call time: a plugin
  * running inside a host engine that owns every byte of the GPU's memory
@@ -154,8 +154,8 @@ MOE_API int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const 
  *   Limits: cfg->max_tokens <= 8 and 1 <= m <= cfg->max_tokens; the
  *   workspace moe_v41_workspace_bytes(cfg) would need must fit in
  *   MOE_V41_NOALLOC_SCRATCH_BYTES, else MOE_ERR_WORKSPACE (the DeepSeek-V4.1
- *   shape, dim 5120 / inter 2304 / 384 experts / top-6 at 8 tokens, needs about
- *   2.3 MB).  Nothing is allocated: no cudaMalloc, cudaFree or allocating
+ *   shape, dim 5120 / inter 2304 / 384 experts / top-6 at 8 tokens, needs
+ *   356 KB).  Nothing is allocated: no cudaMalloc, cudaFree or allocating
  *   library call.
  *   Set-up: the first call on a device (with that device current) looks up
  *   the array's device address once; make that first call before any stream

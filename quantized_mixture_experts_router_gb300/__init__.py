@@ -127,13 +127,13 @@ def moe_v41_forward(cfg, x, m, router_w, bias, expert_ptrs, shared_kind, sh_w1, 
                                  _p(ws), _nbytes(ws), _s(stream)), "moe_v41_forward")
 
 
-NOALLOC_SCRATCH_BYTES = 4 << 20
+NOALLOC_SCRATCH_BYTES = 512 << 10
 
 
 def moe_v41_forward_noalloc(cfg, x, m, router_w, bias, expert_ptrs, shared_kind, sh_w1, sh_w3, sh_w2, out, topk_w,
                             topk_idx, logits_out=None, status_out=None, stream=None):
     """moe_v41_forward without a workspace: the library's own fixed scratch
-    array (4 MiB per device) is used.  For callers that cannot allocate device
+    array (512 KiB per device) is used.  For callers that cannot allocate device
     memory when they call; see include/moe_v41.h for the limits."""
     _check(lib().moe_v41_forward_noalloc(ctypes.byref(cfg), _p(x), m, _p(router_w), _p(bias), _p(expert_ptrs),
                                          shared_kind, _p(sh_w1), _p(sh_w3), _p(sh_w2), _p(out), _p(topk_w),

@@ -149,15 +149,10 @@ int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const void* ro
   dp.sh2 = static_cast<const uint8_t*>(sh_w2);
   dp.logits = logits_out ? logits_out : reinterpret_cast<float*>(w + L.logits);
   dp.topk_w = topk_w; dp.topk_idx = topk_idx;
-  dp.xq8 = w + L.xq8;
+  dp.sk = reinterpret_cast<float2*>(w + L.sk);
   dp.xu = reinterpret_cast<int*>(w + L.xu);
-  dp.hf = reinterpret_cast<float*>(w + L.hf);
   dp.hu = reinterpret_cast<int*>(w + L.hu);
-  dp.shgu = reinterpret_cast<float*>(w + L.shgu);
   dp.shh = w + L.shh;
-  dp.ep = reinterpret_cast<float*>(w + L.ep);
-  dp.sp = reinterpret_cast<float*>(w + L.sp);
-  dp.cnt = reinterpret_cast<unsigned*>(w + L.cnt);
   dp.plan_w = reinterpret_cast<DecodePlan*>(w + L.plan);
   const int Td = cfg->max_tokens < DECODE_MAX_M ? cfg->max_tokens : DECODE_MAX_M;
   dp.shvec0 = Td * cfg->topk;

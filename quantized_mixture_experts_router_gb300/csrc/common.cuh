@@ -39,7 +39,7 @@ struct Ctrl {
 
 // Routing of a decode call grouped by expert (ascending id), written by the
 // warp that finishes the last router task.
-struct DecodePlan {
+struct alignas(16) DecodePlan {
   int n_exp;                         // distinct experts picked
   int n_pairs;                       // m * topk
   int exp_id[MAXP];                  // ascending
@@ -52,22 +52,13 @@ struct DecodePlan {
 
 // Byte offsets of the workspace regions (all 256-B aligned).
 struct WsLayout {
-  size_t ctrl, plan, cnt, logits, xq8, xu, hf, hu, shgu, shh, ep, sp, total;
-  size_t cnt_words;
+  size_t ctrl, plan, logits, sk, xq8, xu, hu, shh, total;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Bytes of one activation vector of length K in unit layout.
 __host__ __device__ inline size_t unit_bytes(int K) { return (size_t)(K / QK) * 4 * UNIT_WORDS * 4; }
-
-// Counter arrays of the fused decode kernel (words): the shared expert's
-// per-row gate/up pairing, the per-(vector, 32-row) q8_1(h) groups and the
-// per-8-row output groups.
-__host__ __device__ inline int cnt_shpair(int) { return 0; }
-__host__ __device__ inline int cnt_hgrp(int I) { return I; }
-__host__ __device__ inline int cnt_dgrp(int I) { return I + (MAXP + DECODE_MAX_M) * (I / 32); }
-__host__ __device__ inline int cnt_words(int D, int I) { return cnt_dgrp(I) + D / 8; }
 
 inline WsLayout ws_layout(const moe_v41_cfg& c) {
   WsLayout L{};
@@ -78,17 +69,12 @@ inline WsLayout ws_layout(const moe_v41_cfg& c) {
   const size_t vecs = Td * c.topk + Td;  // routed pairs, then the shared expert's tokens
   L.ctrl = take(sizeof(Ctrl));
   L.plan = take(sizeof(DecodePlan));
-  L.cnt_words = (size_t)cnt_words(c.dim, c.inter);
-  L.cnt = take(L.cnt_words * 4);
   L.logits = take(T * c.n_routed * sizeof(float));
+  L.sk = take(Td * c.n_routed * 2 * sizeof(float));  // (score, key) per token and expert, decode path
   L.xq8 = take(T * (c.dim / 32) * Q8_B);
   L.xu = take(T * unit_bytes(c.dim));
-  L.hf = take(vecs * c.inter * sizeof(float));
   L.hu = take(vecs * unit_bytes(c.inter));
-  L.shgu = take(Td * 2 * c.inter * sizeof(float));
   L.shh = take(Td * c.inter * 2);
-  L.ep = take(Td * c.topk * c.dim * sizeof(float));
-  L.sp = take(Td * c.dim * sizeof(float));
   L.total = off;
   return L;
 }
@@ -136,6 +122,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same, letting the hardware suspend the thread for up to `ns`
+// nanoseconds until the phase completes (a blocking wait, not a spin).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -155,9 +154,8 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // status bit once) when the wait ran past the deadline.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t deadline,
                                                   unsigned* status) {
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++spins & 63u) == 0 && globaltimer_ns() > deadline) {
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+    if (globaltimer_ns() > deadline) {
       atomicOr(status, (unsigned)MOE_STATUS_TIMEOUT);
       return false;
     }
@@ -290,6 +288,21 @@ __device__ __forceinline__ float q3k_unit_dot(const uint8_t* blk, int c, const X
   return half_bits_to_float(dbits) * acc;
 }
 
+// q8_1 code of v: round-half-away(RN(v / d)), the f32 decision of the q8_1
+// rule, mostly without a division.  y = v * RN(1/d) is within 2^-22 |y| of
+// RN(v / d) (1/d and the product are each rounded once, 2^-24 relative, and
+// v / d itself is within 2^-24 of its rounding); when y lies farther than
+// 2^-19 max(|y|, 1) from every half-integer both round to the same integer.
+// Otherwise (a few values in 10^4), or when 1/d overflowed, the quotient is
+// computed exactly.
+__device__ __forceinline__ int q8_code(float v, float d, float rd) {
+  const float y = v * rd;
+  const float a = fabsf(y);
+  const float f = a - floorf(a);
+  if (a < 1.0e30f && fabsf(f - 0.5f) > 0x1.0p-19f * fmaxf(a, 1.0f)) return (int)copysignf(floorf(a + 0.5f), y);
+  return (int)roundf(__fdiv_rn(v, d));
+}
+
 // ------------------------------------------------------------------ q8_1 (warp)
 // One warp quantises one q8_1 block of 32 values (lane i holds value i):
 // d = amax/127, q = round-half-away(v/d), decisions in f32.  Writes the
@@ -302,7 +315,7 @@ __device__ __forceinline__ void q8_block_warp(float v, int qb, uint8_t* q8, int*
 #pragma unroll
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float d = __fdiv_rn(amax, 127.0f);
-  const int q = amax == 0.0f ? 0 : (int)roundf(__fdiv_rn(v, d));
+  const int q = amax == 0.0f ? 0 : q8_code(v, d, __frcp_rn(d));
   int s = q, s16;
 #pragma unroll
   for (int o = 8; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);  // sums within 16-lane halves
@@ -334,6 +347,55 @@ __device__ __forceinline__ void q8_block_warp(float v, int qb, uint8_t* q8, int*
       u[20 + j] = s16;
     }
   }
+}
+
+// The same quantisation of one block by ONE thread (no shuffles, so a warp
+// quantises 32 blocks at once): x32 = 32 bf16 values (16-B aligned), qb = the
+// block's index within its vector.  Bit-identical to q8_block_warp: the same
+// f32 operations in the same order for every value; amax and the integer sums
+// do not depend on the order.
+__device__ __forceinline__ void q8_block_thread(const uint16_t* x32, int qb, int* units) {
+  const uint4* xp = reinterpret_cast<const uint4*>(x32);
+  uint32_t raw[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = xp[i];
+    raw[4 * i + 0] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(raw[i])), fabsf(bf16hi(raw[i]))));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const float rd = __frcp_rn(d);
+  uint32_t word[8];
+  int s0 = 0, s1 = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    uint32_t wd = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int e = 4 * w + b;
+      const uint32_t r = raw[e >> 1];
+      const float v = (e & 1) ? bf16hi(r) : bf16lo(r);
+      const int q = amax == 0.0f ? 0 : q8_code(v, d, rd);
+      wd |= (uint32_t)(q & 0xFF) << (8 * b);
+      if (w < 4) s0 += q; else s1 += q;
+    }
+    word[w] = wd;
+  }
+  const float dq = __half2float(__float2half_rn(d));
+  const int b256 = qb >> 3, hj = qb & 7, h = hj >> 2, j = hj & 3;
+  int* u0 = units + ((size_t)b256 * 4 + 2 * h) * UNIT_WORDS;
+  int* u1 = u0 + UNIT_WORDS;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    u0[4 * j + w] = (int)word[w];
+    u1[4 * j + w] = (int)word[4 + w];
+  }
+  u0[16 + j] = __float_as_int(dq);
+  u1[16 + j] = __float_as_int(dq);
+  u0[20 + j] = s0;
+  u1[20 + j] = s1;
 }
 
 }  // namespace moe

@@ -42,22 +42,20 @@ struct DecodeParams {
   const uint8_t* sh3;
   const uint8_t* sh2;
   float* logits;             // [m, N]
+  float2* sk;                // (fast score, fast key) [m, N]
   float* topk_w;             // [m, k]
   int* topk_idx;             // [m, k]
-  uint8_t* xq8;              // q8_1 blocks of x
-  int* xu;                   // unit layout of q8_1(x)
-  float* hf;                 // h in f32, one row of I per vector (pairs, then shared tokens)
-  int* hu;                   // unit layout of q8_1(h), one per vector
-  float* shgu;               // bf16 shared expert: g and u per token
+  int* xu;                   // unit layout of q8_1(x) (when not kept in shared memory)
+  int* hu;                   // unit layout of q8_1(h), one per vector (pairs, then shared tokens)
   uint8_t* shh;              // bf16 shared expert: h [m, I] bf16
-  float* ep;                 // E of each pair [pairs, D]
-  float* sp;                 // shared expert output [m, D]
-  unsigned* cnt;             // counter arrays
   DecodePlan* plan_w;
   int shvec0;                // first vector index of the shared expert's tokens
   float* out;                // f32 [m, D]
   Ctrl* ctrl;
   unsigned long long timeout_ns;
+  // shared-memory plan of the launch (set by launch_decode_layer); a cache
+  // offset of 0 means "not cached, read from global memory"
+  uint32_t sm_ctl, sm_plan, sm_items, item_bytes, sm_sel, sm_xb, sm_ep, ep_bytes, sm_x, sm_hr, sm_hs, smem_bytes;
 };
 
 int launch_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols, void* q8, cudaStream_t s);

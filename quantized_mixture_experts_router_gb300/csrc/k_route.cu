@@ -30,10 +30,12 @@ __global__ void k_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols,
 }
 
 __global__ void k_select(SelectParams p) {
+  extern __shared__ __align__(16) float sel_scratch[];
   const int warps = (gridDim.x * blockDim.x) >> 5;
+  float* scratch = sel_scratch + (size_t)(threadIdx.x >> 5) * 3 * p.N;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < p.m; t += warps)
-    route_token_warp(p.logits + (size_t)t * p.N, p.bias, p.N, p.k, p.gate_temp, p.norm, p.route_scale,
-                     p.topk_w + (size_t)t * p.k, p.topk_idx + (size_t)t * p.k, &p.ctrl->status);
+    route_token_warp(p.logits + (size_t)t * p.N, nullptr, p.bias, p.N, p.k, p.gate_temp, p.norm, p.route_scale,
+                     p.topk_w + (size_t)t * p.k, p.topk_idx + (size_t)t * p.k, &p.ctrl->status, scratch);
 }
 
 // ---------------------------------------------- router + selection (m <= 8)
@@ -108,10 +110,12 @@ __global__ void __launch_bounds__(256) k_route_decode(RouteParams p) {
   if (threadIdx.x == 0) {
     p.ctrl->route_arrive = 0u;  // ready for the next call
   }
+  extern __shared__ __align__(16) float sel_scratch[];
   const int warp = threadIdx.x >> 5;
   if (warp < p.m)
-    route_token_warp(p.logits + (size_t)warp * p.N, p.bias, p.N, p.k, p.gate_temp, p.norm, p.route_scale,
-                     p.topk_w + (size_t)warp * p.k, p.topk_idx + (size_t)warp * p.k, &p.ctrl->status);
+    route_token_warp(p.logits + (size_t)warp * p.N, nullptr, p.bias, p.N, p.k, p.gate_temp, p.norm, p.route_scale,
+                     p.topk_w + (size_t)warp * p.k, p.topk_idx + (size_t)warp * p.k, &p.ctrl->status,
+                     sel_scratch + (size_t)warp * 3 * p.N);
 }
 
 // ------------------------------------------------------------- launchers
@@ -125,16 +129,22 @@ int launch_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols, void* 
 }
 
 int launch_select(const SelectParams& p, cudaStream_t s) {
-  long blocks = ((long)p.m * 32 + 255) / 256;
-  if (blocks > 152L * 8) blocks = 152L * 8;
-  k_select<<<(unsigned)blocks, 256, 0, s>>>(p);
+  constexpr int WPB = 4;  // warps (tokens) per block
+  const size_t smem = WPB * select_scratch_bytes(p.N);
+  long blocks = ((long)p.m + WPB - 1) / WPB;
+  if (blocks > 152L * 16) blocks = 152L * 16;
+  k_select<<<(unsigned)blocks, WPB * 32, smem, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int launch_route_decode(const RouteParams& p, cudaStream_t s) {
   const long warps = (long)p.N + (long)p.m * (p.D / 32);
   const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
-  k_route_decode<<<blocks, 256, 0, s>>>(p);
+  const size_t smem = (size_t)p.m * select_scratch_bytes(p.N);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(k_route_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  k_route_decode<<<blocks, 256, smem, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

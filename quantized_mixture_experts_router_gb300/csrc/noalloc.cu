@@ -69,9 +69,8 @@ extern "C" int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, in
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* w = static_cast<uint8_t*>(base);
   // The array keeps whatever the previous call left: clear the control block
-  // and the counters this call starts from.
+  // (status word and counters) this call starts from.
   if (cudaMemsetAsync(w + L.ctrl, 0, sizeof(Ctrl), s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemsetAsync(w + L.cnt, 0, L.cnt_words * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   DecodeParams dp{};
   dp.m = m; dp.D = c.dim; dp.I = c.inter; dp.N = c.n_routed; dp.k = c.topk;
@@ -87,15 +86,10 @@ extern "C" int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, in
   dp.sh2 = static_cast<const uint8_t*>(sh_w2);
   dp.logits = logits_out ? logits_out : reinterpret_cast<float*>(w + L.logits);
   dp.topk_w = topk_w; dp.topk_idx = topk_idx;
-  dp.xq8 = w + L.xq8;
+  dp.sk = reinterpret_cast<float2*>(w + L.sk);
   dp.xu = reinterpret_cast<int*>(w + L.xu);
-  dp.hf = reinterpret_cast<float*>(w + L.hf);
   dp.hu = reinterpret_cast<int*>(w + L.hu);
-  dp.shgu = reinterpret_cast<float*>(w + L.shgu);
   dp.shh = w + L.shh;
-  dp.ep = reinterpret_cast<float*>(w + L.ep);
-  dp.sp = reinterpret_cast<float*>(w + L.sp);
-  dp.cnt = reinterpret_cast<unsigned*>(w + L.cnt);
   dp.plan_w = reinterpret_cast<DecodePlan*>(w + L.plan);
   dp.shvec0 = c.max_tokens * c.topk;
   dp.out = out;

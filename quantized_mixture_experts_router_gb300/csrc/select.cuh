@@ -52,7 +52,8 @@ static __device__ __forceinline__ float score_fast(float z, float T) {
   return __fsqrt_rn(log1pf(expf(t)));
 }
 
-constexpr int SEL_PER_LANE = MAX_N / 32;
+// Scratch one warp needs in shared memory for one token: 3 * N words.
+__host__ __device__ inline size_t select_scratch_bytes(int N) { return (size_t)3 * N * 4; }
 
 // One token's routing by one warp.
 //
@@ -64,31 +65,41 @@ constexpr int SEL_PER_LANE = MAX_N / 32;
 // ulp.  When the fast top-k is separated by more than 2 eps from every
 // neighbour it is the exact top-k in the exact order, and no f64 work is
 // done.  Otherwise every expert within 2 eps of the k-th fast key is
-// re-scored with score_exact (one candidate per lane per pass) and the picks
-// are taken on the exact keys: the exact top-k is always inside that set.
-// Weights use the scores of the path taken (fast scores differ from the exact
-// ones by < 2^-20 relative).
-static __device__ __noinline__ void route_token_warp(const float* __restrict__ z, const float* __restrict__ bias, int N, int k,
-                                 float T, int norm, float route_scale, float* w_out, int* idx_out, unsigned* status) {
+// re-scored with score_exact (one candidate per lane) and the picks are taken
+// on the exact keys: the exact top-k is always inside that set.  Weights use
+// the scores of the path taken (fast scores are within 2^-20 relative).
+// scratch: select_scratch_bytes(N) bytes of shared memory for this warp.
+// sk (may be NULL): the (score_fast, fast key) pairs already computed for this
+// token, exactly as below.  pick_id / pick_w (may be NULL): shared-memory
+// copies of the picks.
+static __device__ __noinline__ void route_token_warp(const float* __restrict__ z, const float2* __restrict__ sk,
+                                                     const float* __restrict__ bias, int N, int k, float T, int norm,
+                                                     float route_scale, float* w_out, int* idx_out, unsigned* status,
+                                                     float* scratch, int* pick_id = nullptr,
+                                                     float* pick_w = nullptr) {
   const int lane = threadIdx.x & 31;
-  float kf[SEL_PER_LANE], sf[SEL_PER_LANE];
+  float* skey = scratch;
+  float* ssc = scratch + N;
+  int* slist = reinterpret_cast<int*>(scratch + 2 * N);
   bool any_nan = false;
   float smax = 0.f, kmax = 0.f;
-#pragma unroll
-  for (int i = 0; i < SEL_PER_LANE; ++i) {
-    const int e = lane + 32 * i;
-    float key = -INFINITY, sc = 0.f;
-    if (e < N) {
+  for (int e = lane; e < N; e += 32) {
+    float sc, key;
+    if (sk) {
+      const float2 v = __ldcg(sk + e);
+      sc = v.x;
+      key = v.y;
+    } else {
       sc = score_fast(__ldcg(z + e), T);
       key = __fadd_rn(sc, __ldg(bias + e));
-      any_nan |= (key != key);
-      if (key == key) {
-        smax = fmaxf(smax, fabsf(sc));
-        kmax = fmaxf(kmax, fabsf(key));
-      }
     }
-    kf[i] = key;
-    sf[i] = sc;
+    any_nan |= (key != key);
+    if (key == key) {
+      smax = fmaxf(smax, fabsf(sc));
+      kmax = fmaxf(kmax, fabsf(key));
+    }
+    skey[e] = key;
+    ssc[e] = sc;
   }
   if (__any_sync(0xffffffffu, any_nan) && lane == 0) atomicOr(status, (unsigned)MOE_STATUS_NAN_KEY);
 #pragma unroll
@@ -96,86 +107,76 @@ static __device__ __noinline__ void route_token_warp(const float* __restrict__ z
     smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
     kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
+  __syncwarp();
   const float eps = 0x1.0p-18f * (smax + kmax) + 0x1.0p-126f;
 
-  // fast top-(k+1) in rank order (ties by id)
+  // fast top-(k+1) in rank order (ties by id); taken entries: bit i of the
+  // lane's mask stands for expert lane + 32 i
   uint32_t taken = 0;
-  float prev_key = 0.f;
+  float prev_key = 0.f, kth_key = 0.f;
   bool resolved = true;
   int picked_id[MAX_TOPK];
   float picked_s[MAX_TOPK];
-  float kth_key = 0.f;
   const int rounds = k < N ? k + 1 : k;
   for (int r = 0; r < rounds; ++r) {
     unsigned long long best = 0;
-    float bk = 0.f, bs = 0.f;
-#pragma unroll
-    for (int i = 0; i < SEL_PER_LANE; ++i) {
-      const int e = lane + 32 * i;
-      if (e < N && !(taken >> i & 1u)) {
-        const unsigned long long rk = rank_key(kf[i], e);
-        if (rk > best) { best = rk; bk = kf[i]; bs = sf[i]; }
+    for (int e = lane, i = 0; e < N; e += 32, ++i) {
+      if (!(taken >> i & 1u)) {
+        const unsigned long long rk = rank_key(skey[e], e);
+        best = rk > best ? rk : best;
       }
     }
     const unsigned long long wmax = warp_max_u64(best);
     const int win = (int)(0xFFFFFFFFu - (uint32_t)(wmax & 0xFFFFFFFFu));
-    const float wk = __shfl_sync(0xffffffffu, bk, win & 31);
-    const float ws = __shfl_sync(0xffffffffu, bs, win & 31);
+    const float wk = skey[win];
     if ((win & 31) == lane) taken |= 1u << (win >> 5);
     // neighbouring keys must be separated by more than 2 eps (NaN never is)
     if (r > 0 && !(prev_key - wk > 2.0f * eps)) resolved = false;
     prev_key = wk;
     if (r < k) {
       picked_id[r] = win;
-      picked_s[r] = ws;
+      picked_s[r] = ssc[win];
       kth_key = wk;
     }
   }
 
   if (!resolved) {
-    // exact keys for every expert within 2 eps of the k-th fast key
+    // candidates: every expert within 2 eps of the k-th fast key
     const bool kth_nan = kth_key != kth_key;
     const float thresh = kth_key - 2.0f * eps;
-    uint32_t pend = 0;
-#pragma unroll
-    for (int i = 0; i < SEL_PER_LANE; ++i) {
-      const int e = lane + 32 * i;
-      if (e < N && (kth_nan || !(kf[i] < thresh))) pend |= 1u << i;
+    int nc = 0;
+    for (int base = 0; base < N; base += 32) {
+      const int e = base + lane;
+      const bool c = e < N && (kth_nan || !(skey[e] < thresh));
+      const unsigned bal = __ballot_sync(0xffffffffu, c);
+      if (c) slist[nc + __popc(bal & ((1u << lane) - 1u))] = e;
+      nc += __popc(bal);
     }
-    uint32_t cand = pend;
-    float se[SEL_PER_LANE];
-#pragma unroll
-    for (int i = 0; i < SEL_PER_LANE; ++i) se[i] = 0.f;
-    // one candidate per lane per pass
-    while (__any_sync(0xffffffffu, pend != 0)) {
-      const int i = pend ? __ffs(pend) - 1 : -1;
-      float v = 0.f;
-      if (i >= 0) {
-        const int e = lane + 32 * i;
-        v = score_exact(__ldcg(z + e), T);
-        pend &= pend - 1;
-      }
-#pragma unroll
-      for (int q = 0; q < SEL_PER_LANE; ++q)
-        if (q == i) { se[q] = v; kf[q] = __fadd_rn(v, __ldg(bias + lane + 32 * q)); }
+    __syncwarp();
+    for (int c = lane; c < nc; c += 32) {
+      const int e = slist[c];
+      const float sx = score_exact(__ldcg(z + e), T);
+      ssc[e] = sx;
+      skey[e] = __fadd_rn(sx, __ldg(bias + e));
     }
+    __syncwarp();
+    uint32_t used = 0;  // bit c of lane's mask: candidate lane + 32 c taken
     for (int r = 0; r < k; ++r) {
       unsigned long long best = 0;
-      float bs = 0.f;
-#pragma unroll
-      for (int i = 0; i < SEL_PER_LANE; ++i) {
-        const int e = lane + 32 * i;
-        if (cand >> i & 1u) {
+      for (int c = lane, i = 0; c < nc; c += 32, ++i) {
+        if (!(used >> i & 1u)) {
           // rank keys are never 0, so a NaN candidate still beats "none left"
-          const unsigned long long rk = rank_key(kf[i], e);
-          if (rk > best) { best = rk; bs = se[i]; }
+          const int e = slist[c];
+          const unsigned long long rk = rank_key(skey[e], e);
+          best = rk > best ? rk : best;
         }
       }
       const unsigned long long wmax = warp_max_u64(best);
       const int win = (int)(0xFFFFFFFFu - (uint32_t)(wmax & 0xFFFFFFFFu));
-      picked_s[r] = __shfl_sync(0xffffffffu, bs, win & 31);
       picked_id[r] = win;
-      if ((win & 31) == lane) cand &= ~(1u << (win >> 5));
+      picked_s[r] = ssc[win];
+      for (int c = lane, i = 0; c < nc; c += 32, ++i)
+        if (slist[c] == win) used |= 1u << i;
     }
   }
   if (lane == 0) {
@@ -188,10 +189,110 @@ static __device__ __noinline__ void route_token_warp(const float* __restrict__ z
       for (int r = 0; r < k; ++r) w[r] = __fdiv_rn(w[r], sum);
     }
     for (int r = 0; r < k; ++r) {
-      w_out[r] = __fmul_rn(w[r], route_scale);
+      const float wr = __fmul_rn(w[r], route_scale);
+      w_out[r] = wr;
       idx_out[r] = picked_id[r];
+      if (pick_id) {
+        pick_id[r] = picked_id[r];
+        pick_w[r] = wr;
+      }
     }
   }
+  __syncwarp();
+}
+
+// The same routing with up to 12 keys per lane held in registers (N <= 384),
+// for the latency-critical single-warp use: every load is issued before any
+// is used, and the picks travel by shuffles.  sk: the fast (score, key) pairs.
+// Falls back to route_token_warp (shared-memory scratch, exact re-scoring)
+// when the fast keys do not separate the picks.  Same results.
+static __device__ __noinline__ void route_token_warp_r12(const float* __restrict__ z, const float2* __restrict__ sk,
+                                                         const float* __restrict__ bias, int N, int k, float T,
+                                                         int norm, float route_scale, float* w_out, int* idx_out,
+                                                         unsigned* status, float* scratch, int* pick_id,
+                                                         float* pick_w) {
+  constexpr int PL = 12;
+  const int lane = threadIdx.x & 31;
+  float kf[PL], sf[PL];
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int e = lane + 32 * i;
+    const float2 v = e < N ? __ldcg(sk + e) : make_float2(0.f, 0.f);
+    sf[i] = v.x;
+    kf[i] = v.y;
+  }
+  bool any_nan = false;
+  float smax = 0.f, kmax = 0.f;
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    if (lane + 32 * i < N) {
+      any_nan |= (kf[i] != kf[i]);
+      if (kf[i] == kf[i]) {
+        smax = fmaxf(smax, fabsf(sf[i]));
+        kmax = fmaxf(kmax, fabsf(kf[i]));
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, any_nan) && lane == 0) atomicOr(status, (unsigned)MOE_STATUS_NAN_KEY);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+    kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  const float eps = 0x1.0p-18f * (smax + kmax) + 0x1.0p-126f;
+  uint32_t taken = 0;
+  float prev_key = 0.f;
+  bool resolved = true;
+  int pid[MAX_TOPK];
+  float ps[MAX_TOPK];
+#pragma unroll
+  for (int q = 0; q < MAX_TOPK; ++q) { pid[q] = 0; ps[q] = 0.f; }
+  const int rounds = k < N ? k + 1 : k;
+  for (int r = 0; r < rounds; ++r) {
+    unsigned long long best = 0;
+    float bk = 0.f, bs = 0.f;
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < N && !(taken >> i & 1u)) {
+        const unsigned long long rk = rank_key(kf[i], e);
+        if (rk > best) { best = rk; bk = kf[i]; bs = sf[i]; }
+      }
+    }
+    const unsigned long long wmax = warp_max_u64(best);
+    const int win = (int)(0xFFFFFFFFu - (uint32_t)(wmax & 0xFFFFFFFFu));
+    const float wk = __shfl_sync(0xffffffffu, bk, win & 31);
+    const float ws = __shfl_sync(0xffffffffu, bs, win & 31);
+    if ((win & 31) == lane) taken |= 1u << (win >> 5);
+    if (r > 0 && !(prev_key - wk > 2.0f * eps)) resolved = false;
+    prev_key = wk;
+#pragma unroll
+    for (int q = 0; q < MAX_TOPK; ++q)
+      if (q == r) { pid[q] = win; ps[q] = ws; }
+  }
+  if (!resolved) {
+    route_token_warp(z, sk, bias, N, k, T, norm, route_scale, w_out, idx_out, status, scratch, pick_id, pick_w);
+    return;
+  }
+  if (lane == 0) {
+    float sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < MAX_TOPK; ++q)
+      if (q < k) sum = __fadd_rn(sum, ps[q]);
+    sum = __fadd_rn(sum, 1e-20f);
+    const bool nrm = norm && k > 1;
+#pragma unroll
+    for (int q = 0; q < MAX_TOPK; ++q) {
+      if (q < k) {
+        const float wv = __fmul_rn(nrm ? __fdiv_rn(ps[q], sum) : ps[q], route_scale);
+        w_out[q] = wv;
+        idx_out[q] = pid[q];
+        pick_id[q] = pid[q];
+        pick_w[q] = wv;
+      }
+    }
+  }
+  __syncwarp();
 }
 
 }  // namespace moe
