@@ -61,6 +61,30 @@ RouteParams route_params(const moe_v41_cfg* c, const void* x, int m, const void*
   return p;
 }
 
+PrefillParams prefill_params(const moe_v41_cfg* c, const void* x, int m, const void* router_w, const float* bias,
+                             const uint64_t* expert_ptrs, int shared_kind, const void* sh1, const void* sh3,
+                             const void* sh2, float* out, float* topk_w, int32_t* topk_idx, float* logits,
+                             uint8_t* ws, const WsLayout& L) {
+  PrefillParams p{};
+  p.m = m; p.D = c->dim; p.I = c->inter; p.N = c->n_routed; p.k = c->topk; p.norm = c->norm_topk_prob != 0;
+  p.gate_temp = c->gate_temp; p.route_scale = c->route_scale; p.swiglu_limit = c->swiglu_limit;
+  p.shared_kind = shared_kind;
+  p.x = static_cast<const uint16_t*>(x);
+  p.router_w = static_cast<const uint16_t*>(router_w);
+  p.bias = bias;
+  p.expert_ptrs = reinterpret_cast<const unsigned long long*>(expert_ptrs);
+  p.sh1 = static_cast<const uint8_t*>(sh1);
+  p.sh3 = static_cast<const uint8_t*>(sh3);
+  p.sh2 = static_cast<const uint8_t*>(sh2);
+  p.logits = logits ? logits : reinterpret_cast<float*>(ws + L.logits);
+  p.topk_w = topk_w; p.topk_idx = topk_idx; p.out = out;
+  p.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  p.pw = ws + L.pre;
+  p.L = L.P;
+  p.timeout_ns = timeout_ns(c);
+  return p;
+}
+
 }  // namespace
 
 extern "C" {
@@ -110,7 +134,9 @@ int moe_v41_route(const moe_v41_cfg* cfg, const void* x, int m, const void* rout
     RouteParams p = route_params(cfg, x, m, router_w, bias, logits_out, topk_w, topk_idx, w, L);
     return launch_route_decode(p, (cudaStream_t)stream);
   }
-  return MOE_ERR_ARG;  // the prefill router is added with the prefill path
+  PrefillParams p = prefill_params(cfg, x, m, router_w, bias, nullptr, MOE_SHARED_BF16, nullptr, nullptr, nullptr,
+                                   nullptr, topk_w, topk_idx, logits_out, w, L);
+  return launch_prefill_route(p, (cudaStream_t)stream);
 }
 
 int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w, const float* bias,
@@ -129,7 +155,12 @@ int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const void* ro
   const WsLayout L = ws_layout(*cfg);
   uint8_t* w = static_cast<uint8_t*>(ws);
   cudaStream_t s = (cudaStream_t)stream;
-  if (!use_decode(cfg, m)) return MOE_ERR_ARG;  // the prefill kernels come with the prefill path
+  if (!use_decode(cfg, m)) {
+    if (!prefill_possible(*cfg)) return MOE_ERR_ARG;
+    PrefillParams p = prefill_params(cfg, x, m, router_w, bias, expert_ptrs, shared_kind, sh_w1, sh_w3, sh_w2, out,
+                                     topk_w, topk_idx, logits_out, w, L);
+    return launch_prefill(p, s);
+  }
   if (m > DECODE_MAX_M) return MOE_ERR_ARG;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;

@@ -50,15 +50,65 @@ struct alignas(16) DecodePlan {
   unsigned long long exp_ptr[MAXP][3];    // w1, w3, w2 of each distinct expert (0 = skip)
 };
 
+// Prefill tiling: weight rows per GEMM tile, columns (pairs or tokens) per
+// tile, K values per pipeline stage, tokens per grouping chunk.
+constexpr int PF_TM = 128;
+constexpr int PF_TN = 256;     // down projection, router and shared-expert GEMMs
+constexpr int PF_TN_GU = 128;  // routed gate/up GEMM (hi/lo split operands)
+constexpr int PF_KC = 64;
+constexpr int PF_GCH = 64;
+
+// Byte offsets of the prefill regions, relative to the prefill base.
+struct PrefillLayout {
+  size_t x16h, x16l, chunk, offsets, expert_ok, pair_tok, pair_w, pos_of, pos_sh, n_tiles, gu_tiles, dn_tiles, h16,
+      ep, hs, sp, total;
+  size_t max_gu_tiles, max_dn_tiles;  // bounds on the column tiles over all experts
+};
+
 // Byte offsets of the workspace regions (all 256-B aligned).
 struct WsLayout {
-  size_t ctrl, plan, logits, sk, xq8, xu, hu, shh, total;
+  size_t ctrl, plan, logits, sk, xq8, xu, hu, shh, pre, total;
+  PrefillLayout P;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Bytes of one activation vector of length K in unit layout.
 __host__ __device__ inline size_t unit_bytes(int K) { return (size_t)(K / QK) * 4 * UNIT_WORDS * 4; }
+
+inline PrefillLayout prefill_layout(const moe_v41_cfg& c) {
+  PrefillLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+  const size_t T = (size_t)c.max_tokens, P = T * c.topk, V = P + T;  // pairs, plus the K-quant shared expert's
+  const size_t NE = (size_t)c.n_routed + 1;
+  const size_t nch = (T + PF_GCH - 1) / PF_GCH;
+  L.max_gu_tiles = NE + V / PF_TN_GU + 1;
+  L.max_dn_tiles = NE + V / PF_TN + 1;
+  L.x16h = take(T * c.dim * 2);
+  L.x16l = take(T * c.dim * 2);
+  L.chunk = take(nch * NE * 4);
+  L.offsets = take((NE + 1) * 4);
+  L.expert_ok = take(NE * 4);
+  L.pair_tok = take(V * 4);
+  L.pair_w = take(V * 4);
+  L.pos_of = take(P * 4);
+  L.pos_sh = take(T * 4);
+  L.n_tiles = take(2 * 4);
+  L.gu_tiles = take(L.max_gu_tiles * (c.inter / PF_TM) * 16);
+  L.dn_tiles = take(L.max_dn_tiles * (c.dim / PF_TM) * 16);
+  L.h16 = take(V * c.inter * 2);
+  L.ep = take(V * c.dim * 4);
+  L.hs = take(T * c.inter * 2);
+  L.sp = take(T * c.dim * 4);
+  L.total = off;
+  return L;
+}
+
+// Whether a configuration can take the prefill kernels.
+inline bool prefill_possible(const moe_v41_cfg& c) {
+  return c.path == MOE_PATH_PREFILL || (c.path == MOE_PATH_AUTO && c.max_tokens > DECODE_MAX_M);
+}
 
 inline WsLayout ws_layout(const moe_v41_cfg& c) {
   WsLayout L{};
@@ -71,10 +121,14 @@ inline WsLayout ws_layout(const moe_v41_cfg& c) {
   L.plan = take(sizeof(DecodePlan));
   L.logits = take(T * c.n_routed * sizeof(float));
   L.sk = take(Td * c.n_routed * 2 * sizeof(float));  // (score, key) per token and expert, decode path
-  L.xq8 = take(T * (c.dim / 32) * Q8_B);
-  L.xu = take(T * unit_bytes(c.dim));
+  L.xq8 = take(Td * (c.dim / 32) * Q8_B);
+  L.xu = take(Td * unit_bytes(c.dim));
   L.hu = take(vecs * unit_bytes(c.inter));
   L.shh = take(Td * c.inter * 2);
+  if (prefill_possible(c)) {
+    L.P = prefill_layout(c);
+    L.pre = take(L.P.total);
+  }
   L.total = off;
   return L;
 }

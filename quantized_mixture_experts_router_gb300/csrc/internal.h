@@ -58,11 +58,35 @@ struct DecodeParams {
   uint32_t sm_ctl, sm_plan, sm_items, item_bytes, sm_sel, sm_xb, sm_ep, ep_bytes, sm_x, sm_hr, sm_hs, smem_bytes;
 };
 
+struct PrefillParams {
+  int m, D, I, N, k, norm;
+  float gate_temp, route_scale, swiglu_limit;
+  int shared_kind;
+  const uint16_t* x;         // bf16 [m, D]
+  const uint16_t* router_w;  // bf16 [N, D]
+  const float* bias;         // [N]
+  const unsigned long long* expert_ptrs;  // [N][3]
+  const uint8_t* sh1;
+  const uint8_t* sh3;
+  const uint8_t* sh2;
+  float* logits;             // [m, N]
+  float* topk_w;             // [m, k]
+  int* topk_idx;             // [m, k]
+  float* out;                // f32 [m, D]
+  Ctrl* ctrl;
+  uint8_t* pw;               // the workspace's prefill region
+  PrefillLayout L;
+  unsigned long long timeout_ns;
+};
+
 int launch_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols, void* q8, cudaStream_t s);
 int launch_select(const SelectParams& p, cudaStream_t s);
 int launch_route_decode(const RouteParams& p, cudaStream_t s);
 int launch_decode_layer(const DecodeParams& p, int num_sms, cudaStream_t s);
 bool decode_fits(int D, int I);
+int launch_prefill(const PrefillParams& p, cudaStream_t s);
+int launch_prefill_route(const PrefillParams& p, cudaStream_t s);
+int prefill_launches(int shared_kind);
 size_t decode_smem_bytes();
 
 }  // namespace moe

@@ -1,0 +1,186 @@
+"""GPU parity of the prefill path (tensor-core GEMMs over expert-grouped
+tokens) against the oracle, through the C-ABI.
+
+Same bars as the decode path: top-k indices bit-exact on identical f32
+logits; outputs and routing weights within 2e-3 relative L2 and max-abs <=
+1e-2 x RMS of the oracle output.  The tiny shapes are checked on every token;
+the full-size prefill workloads (512 tokens with hot experts, 4096 tokens
+with x50 outlier rows) on sampled tokens, plus properties of every token."""
+import numpy as np
+import pytest
+
+import oracle
+import synth.workloads as W
+from _helpers import assert_close, gpu_forward, lib_cfg, oracle_for
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import quantized_mixture_experts_router_gb300 as Q  # noqa: E402
+from synth.device import stage_layer  # noqa: E402
+
+
+def _check(w, layer, res, tokens=None):
+    """Oracle on the GPU's logits for the given tokens (all by default)."""
+    sel = slice(None) if tokens is None else np.asarray(tokens)
+    picked = np.unique(res["topk_idx"][sel])
+    r = oracle_for(w, layer, given_logits=res["logits"], tokens=tokens, picked=picked)
+    np.testing.assert_array_equal(res["topk_idx"][sel], r.topk_idx)
+    ew = assert_close(res["topk_w"][sel], r.topk_w, "routing weights")
+    eo = assert_close(res["out"][sel], r.out, "output")
+    print(f"\n{w.name} m={w.m}: weights rel L2 {ew[0]:.2e} max/RMS {ew[1]:.2e}; "
+          f"output rel L2 {eo[0]:.2e} max/RMS {eo[1]:.2e}")
+    # router logits against the oracle's f64 dot.  The tensor cores' f32
+    # accumulation is not a sequential IEEE sum: bound the error by
+    # 2^-14 of sum_k |x_k w_k| (about 8x the largest error seen).
+    x = W.x_bf16(w, layer)[sel]
+    R = W.router_bf16(w, layer)
+    zr = oracle.router_logits(x, R)
+    bf = lambda a: (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    cond = np.abs(bf(x)) @ np.abs(bf(R)).T
+    err = np.abs(res["logits"][sel] - zr)
+    assert np.all(err <= 2.0 ** -14 * cond + 1e-6), float((err / (cond + 1e-30)).max())
+    return r
+
+
+@pytest.mark.parametrize("m", [1, 4, 9, 100, 700])
+def test_tiny_prefill(m):
+    w = W.WORKLOADS["tiny"].with_(m=m)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    res = gpu_forward(dl, path=Q.MOE_PATH_PREFILL)
+    assert res["status"] == 0
+    _check(w, 0, res)
+
+
+def test_tiny_prefill_auto_path_above_eight():
+    w = W.WORKLOADS["tiny"].with_(m=33)
+    dl = stage_layer(w, 1, experts_on_gpu=False)
+    res = gpu_forward(dl)  # AUTO: 33 tokens take the prefill kernels
+    assert res["status"] == 0
+    _check(w, 1, res)
+
+
+def test_tiny_prefill_many_column_tiles():
+    """Two hot experts take nearly every token: several 256-pair column
+    tiles per expert, the last one ragged."""
+    w = W.WORKLOADS["tiny"].with_(m=1100, hot_experts=2, hot_bias=3.0)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    res = gpu_forward(dl, path=Q.MOE_PATH_PREFILL)
+    counts = np.bincount(res["topk_idx"].ravel(), minlength=w.n_routed)
+    assert counts.max() > 3 * 256
+    _check(w, 0, res)
+
+
+@pytest.mark.parametrize("variant", ["topk1", "no_norm", "no_clip", "kquant_shared", "temp", "outliers", "wide"])
+def test_tiny_prefill_variants(variant):
+    base = W.WORKLOADS["tiny"].with_(m=40)
+    w = {"topk1": base.with_(topk=1), "no_norm": base.with_(norm_topk_prob=False),
+         "no_clip": base.with_(swiglu_limit=0.0), "kquant_shared": base.with_(shared_kind=W.SHARED_KQUANT),
+         "temp": base.with_(gate_temp=0.7, route_scale=2.0), "outliers": base.with_(outlier_frac=0.2),
+         "wide": base.with_(dim=1024, inter=768, n_routed=200, topk=8)}[variant]
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    res = gpu_forward(dl, path=Q.MOE_PATH_PREFILL)
+    assert res["status"] == 0
+    r = _check(w, 0, res)
+    if variant == "outliers":
+        assert r.clipped > 0
+
+
+def test_prefill_matches_decode_path():
+    w = W.WORKLOADS["tiny"].with_(m=8, shared_kind=W.SHARED_KQUANT)
+    dl = stage_layer(w, 2, experts_on_gpu=False)
+    a = gpu_forward(dl, path=Q.MOE_PATH_PREFILL)
+    b = gpu_forward(dl, path=Q.MOE_PATH_DECODE)
+    np.testing.assert_array_equal(a["topk_idx"], b["topk_idx"])
+    assert_close(a["out"], b["out"], "prefill vs decode")
+
+
+def test_prefill_deterministic():
+    w = W.WORKLOADS["tiny"].with_(m=300)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    a = gpu_forward(dl, path=Q.MOE_PATH_PREFILL)
+    b = gpu_forward(dl, path=Q.MOE_PATH_PREFILL, ws=a["ws"])
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["topk_w"], b["topk_w"])
+    np.testing.assert_array_equal(a["topk_idx"], b["topk_idx"])
+
+
+def test_prefill_missing_expert():
+    w = W.WORKLOADS["tiny"].with_(m=50)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    first = gpu_forward(dl, path=Q.MOE_PATH_PREFILL)
+    victim = int(first["topk_idx"][0, 0])
+    dl.expert_ptrs[victim] = 0
+    res = gpu_forward(dl, path=Q.MOE_PATH_PREFILL)
+    assert res["status"] & Q.MOE_STATUS_MISSING_EXPERT
+    keep = [t for t in range(w.m) if victim not in first["topk_idx"][t]]
+    assert keep
+    np.testing.assert_array_equal(res["out"][keep], first["out"][keep])
+    hit = [t for t in range(w.m) if victim in first["topk_idx"][t]]
+    assert np.all(np.isfinite(res["out"][hit]))
+
+
+def test_route_above_eight_tokens():
+    w = W.WORKLOADS["tiny"].with_(m=77)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    cfg = lib_cfg(w)
+    ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    Q.moe_v41_workspace_init(ws)
+    lg = torch.empty((w.m, w.n_routed), dtype=torch.float32, device="cuda")
+    tw = torch.empty((w.m, w.topk), dtype=torch.float32, device="cuda")
+    ti = torch.empty((w.m, w.topk), dtype=torch.int32, device="cuda")
+    Q.moe_v41_route(cfg, dl.x, w.m, dl.router_w, dl.bias, lg, tw, ti, ws)
+    torch.cuda.synchronize()
+    logits = lg.cpu().numpy()
+    zr = oracle.router_logits(W.x_bf16(w, 0), W.router_bf16(w, 0))
+    np.testing.assert_allclose(logits, zr, rtol=1e-4, atol=1e-4)
+    rw, ri, _ = oracle.route_from_logits(oracle.cfg_of(w), logits, W.bias_f32(w, 0))
+    np.testing.assert_array_equal(ti.cpu().numpy(), ri)
+    np.testing.assert_allclose(tw.cpu().numpy(), rw, rtol=2e-6)
+
+
+# ------------------------------------------------------ full-size prefill
+
+def _sample_tokens(w, res, n, must=()):
+    rng = np.random.default_rng(1234)
+    picks = set(int(t) for t in must)
+    picks |= set(int(t) for t in rng.choice(w.m, size=n, replace=False))
+    picks |= {0, w.m - 1}
+    return np.array(sorted(picks), dtype=np.int32)
+
+
+def _full_properties(w, layer, res):
+    assert res["status"] == 0
+    assert np.all(np.isfinite(res["out"]))
+    # every token's selection from the GPU logits, on the host
+    rw, ri, _ = oracle.route_from_logits(oracle.cfg_of(w), res["logits"], W.bias_f32(w, layer))
+    np.testing.assert_array_equal(res["topk_idx"], ri)
+    np.testing.assert_allclose(res["topk_w"], rw, rtol=2e-6)
+    s = res["topk_w"].sum(axis=1)
+    np.testing.assert_allclose(s, w.route_scale, rtol=1e-5)
+
+
+def test_prefill_m512_hot_full_shape():
+    w = W.WORKLOADS["prefill_m512_hot"]
+    dl = stage_layer(w, 0, experts_on_gpu=True)
+    res = gpu_forward(dl)
+    _full_properties(w, 0, res)
+    hot = W.hot_experts(w, 0)
+    counts = np.bincount(res["topk_idx"].ravel(), minlength=w.n_routed)
+    assert counts[hot].sum() > 0.5 * counts.sum()  # imbalanced routing
+    tokens = _sample_tokens(w, res, 24)
+    _check(w, 0, res, tokens=tokens)
+
+
+def test_prefill_m4096_outliers_full_shape():
+    w = W.WORKLOADS["prefill_m4096_outliers"]
+    dl = stage_layer(w, 0, experts_on_gpu=True)
+    res = gpu_forward(dl)
+    _full_properties(w, 0, res)
+    out_rows = W.outlier_rows(w, 0)
+    tokens = _sample_tokens(w, res, 16, must=out_rows[:8])
+    r = _check(w, 0, res, tokens=tokens)
+    assert r.clipped > 0
