@@ -10,8 +10,11 @@ shared expert added last.
 
 Prints one JSON line (rank 0).  `value` is tokens/s through the 40-layer step
 with inputs resident in HBM; `e2e` is the same metric through the C-ABI with
-host buffers copied in and out inside the timed region.  `--impl reference`
-times the CPU oracle instead (the reference arm of this benchmark).
+host buffers copied in and out inside the timed region.  The `prefill` object
+holds the same measurements for the long-prefill workload (one layer call of
+4096 tokens with x50 outlier rows per step), the metric's other size.
+`--impl reference` times the CPU oracle instead (the reference arm of this
+benchmark).
 """
 from __future__ import annotations
 
@@ -50,18 +53,27 @@ def parse():
                     help="expert slots held per layer (default: all; fewer alias experts, for small profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--prefill-workload", default="prefill_m4096_outliers", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--prefill-steps", type=int, default=30)
+    ap.add_argument("--prefill-m", type=int, default=0, help="tokens of the prefill call (default: the workload's)")
+    ap.add_argument("--no-prefill", action="store_true")
     return ap.parse_args()
 
 
 # ------------------------------------------------------------------ utils
 
+BF16_FALLBACK_TFS = 1900.0
+
+
 def peaks():
+    """(HBM GB/s, dense bf16/fp16 TFLOP/s burst, sustained, kind)"""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)) or None, \
+            "measured"
     except Exception:
-        return HBM_FALLBACK_GBS, "fallback"
+        return HBM_FALLBACK_GBS, BF16_FALLBACK_TFS, 1700.0, "fallback"
 
 
 def algorithmic_bytes(w: W.Workload, distinct: float) -> float:
@@ -72,12 +84,54 @@ def algorithmic_bytes(w: W.Workload, distinct: float) -> float:
     return router + distinct * w.expert_bytes + shared + w.m * w.dim * 2 + w.m * w.dim * 4
 
 
-def sources_hash() -> str:
+def algorithmic_flops(w: W.Workload) -> float:
+    """Multiply-adds x 2 the method performs for one layer call: the router
+    GEMV/GEMM, three projections per (token, picked expert), and the shared
+    expert's three projections per token."""
+    router = 2.0 * w.m * w.n_routed * w.dim
+    routed = 2.0 * w.m * w.topk * 3 * w.dim * w.inter
+    shared = 2.0 * w.m * 3 * w.dim * w.inter
+    return router + routed + shared
+
+
+def roofline(w: W.Workload, distinct: float, per_call_ms: float, kernel: str, traffic):
+    """The slower of the byte and the flop bound of one layer call (decode is
+    byte-bound; long prefill is tensor-bound), achieved against it."""
+    hbm, tfs, tfs_sus, kind = peaks()
+    sec = per_call_ms / 1000.0
+    nbytes = algorithmic_bytes(w, distinct)
+    flops = algorithmic_flops(w)
+    t_bytes = nbytes / (hbm * 1e9)
+    t_flops = flops / (tfs * 1e12)
+    if t_bytes >= t_flops:
+        r = {"bound": "hbm", "achieved": nbytes / sec / 1e9, "peak": hbm, "unit": "GB/s",
+             "frac": nbytes / sec / 1e9 / hbm, "peak_kind": f"{kind} (copy bandwidth)"}
+        r["frac_of_8tbs"] = r["achieved"] / 8000.0
+    else:
+        r = {"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tfs, "unit": "TFLOP/s",
+             "frac": flops / sec / 1e12 / tfs,
+             "peak_kind": f"{kind} dense bf16 burst (fp16 runs at the same rate)"}
+        r["hbm_achieved_gbs"] = nbytes / sec / 1e9
+        r["hbm_frac"] = r["hbm_achieved_gbs"] / hbm
+    r.update({"kernel": kernel, "traffic": traffic, "algorithmic_bytes_per_call": nbytes,
+              "algorithmic_flops_per_call": flops, "us_per_call": per_call_ms * 1000.0,
+              "bound_us": max(t_bytes, t_flops) * 1e6})
+    return r
+
+
+KERNEL_SOURCES = {
+    "decode": ["k_decode.cu", "select.cuh", "common.cuh", "internal.h"],
+    "prefill": ["k_prefill.cu", "tc.cuh", "k_route.cu", "select.cuh", "common.cuh", "internal.h"],
+}
+
+
+def sources_hash(kind: str) -> str:
+    """Hash of the sources of one kernel family: a recorded ncu traffic figure
+    is used only while it still describes the code that runs."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_mixture_experts_router_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES[kind]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -92,7 +146,8 @@ def recorded_traffic(workload: str):
         if ":" in line:
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("sources_sha256_16") != sources_hash():
+    kind = "decode" if W.WORKLOADS[workload].m <= 8 else "prefill"
+    if kv.get("sources_sha256_16") != sources_hash(kind):
         return None
     try:
         return float(kv["dram_bytes_per_layer_call"])
@@ -142,10 +197,10 @@ class Clocks:
 
 # ----------------------------------------------------------- oracle (CPU)
 
-def _oracle_inputs(w: W.Workload, layer: int):
+def _oracle_inputs(w: W.Workload, layer: int, tokens):
     import oracle
     x, R, b, sh = W.x_bf16(w, layer), W.router_bf16(w, layer), W.bias_f32(w, layer), W.shared_weights(w, layer)
-    z = oracle.router_logits(x, R)
+    z = oracle.router_logits(x[sorted(set(tokens))], R)
     _, idx, _ = oracle.route_from_logits(oracle.cfg_of(w), z, b)
     experts = [None] * w.n_routed
     for e in np.unique(idx):
@@ -159,21 +214,37 @@ def _oracle_run(w: W.Workload, inp, token: int):
     oracle.moe_layer(oracle.cfg_of(w), x, R, b, experts, w.shared_kind, *sh, tokens=[token], nthreads=1)
 
 
-def cpu_baseline(w: W.Workload, layers_per_step: int, n_units: int, threads: int):
-    """Time the oracle on n_units (layer, token) units spread over `threads`
-    host threads.  Returns (tokens/s, seconds, description)."""
-    units = [(u % w.layers if w.layers > 1 else 0, (u // max(1, w.layers)) % w.m) for u in range(n_units)]
-    layers = sorted(set(l for l, _ in units))
+def cpu_baseline(w: W.Workload, layers_per_step: int, n_units: int, threads: int, target_s: float = 0.0):
+    """Time the oracle, as it stands, on (layer, token) units of the workload
+    spread over `threads` host threads: a fixed sample of distinct units
+    (tokens spread over the batch, layers over the step), repeated until the
+    timed work reaches `target_s` seconds (or exactly n_units units when
+    target_s is 0).  Returns (tokens/s, seconds, units, description)."""
+    base = max(1, min(n_units, threads))
+    stride = max(1, w.m // base)
+    sample = [(u % w.layers if w.layers > 1 else 0, ((u // max(1, w.layers)) * stride) % w.m) for u in range(base)]
+    layers = sorted(set(l for l, _ in sample))
     with ThreadPoolExecutor(min(threads, 8)) as ex:
-        inputs = dict(zip(layers, ex.map(lambda l: _oracle_inputs(w, l), layers)))
-    t0 = time.perf_counter()
-    with ThreadPoolExecutor(threads) as ex:
-        list(ex.map(lambda u: _oracle_run(w, inputs[u[0]], u[1]), units))
-    dt = time.perf_counter() - t0
-    # one step = layers_per_step layer calls of m tokens: tokens/s = units / (layers_per_step) / dt
-    tps = n_units / layers_per_step / dt
-    desc = f"{n_units} (layer, token) units of {w.name} ({len(layers)} layers) on {threads} threads"
-    return tps, dt, desc
+        inputs = dict(zip(layers, ex.map(lambda l: _oracle_inputs(w, l, [t for ll, t in sample if ll == l]),
+                                         layers)))
+
+    def run(n):
+        units = [sample[i % base] for i in range(n)]
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda u: _oracle_run(w, inputs[u[0]], u[1]), units))
+        return time.perf_counter() - t0
+
+    n = n_units
+    if target_s > 0:
+        dt0 = run(base)  # calibration (not reported)
+        n = max(base, min(64 * base, int(math.ceil(target_s / max(dt0, 1e-3))) * base))
+    dt = run(n)
+    # a step moves one token through layers_per_step layer calls
+    tps = n / layers_per_step / dt
+    desc = (f"{n} (layer, token) units of {w.name} cycling over {base} distinct units ({len(layers)} layers, "
+            f"tokens spread over the batch) on {threads} threads; tokens/s = units / layers per step / seconds")
+    return tps, dt, n, desc
 
 
 # ------------------------------------------------------------------- GPU
@@ -284,10 +355,86 @@ def run_ours(args, rank, world, local_rank):
         ms = float(t[0])
         if e2e:
             e2e["ms"] = float(t[1])
+    launches = Q.moe_v41_kernel_launches(cfg, w.m, w.shared_kind)
+    del layers, xs, out, tw, ti, ws
+    torch.cuda.empty_cache()
     return dict(w=w, L=L, K=K, ms=ms, per_call_ms=per_call_ms, distinct=distinct, clocks=clk, e2e=e2e,
-                resident=resident, rotated=rotated, launches_per_call=1 if w.m <= 8 else None,
-                kernel="k_decode_layer (the whole layer call, one launch)" if w.m <= 8 else "prefill kernels",
+                resident=resident, rotated=rotated, launches_per_call=launches,
+                kernel=("k_decode_layer (the whole layer call, one launch)" if launches == 1 else
+                        f"the prefill kernels of one layer call ({launches} launches)"),
                 resident_experts=args.resident_experts)
+
+
+def run_prefill(args, local_rank):
+    """The long-prefill workload: one layer call of m tokens per step on the
+    prefill kernels, timed with events per call; then the same calls through
+    host buffers."""
+    import torch
+    import quantized_mixture_experts_router_gb300 as Q
+    from synth.device import stage_layer
+
+    dev = torch.device("cuda", local_rank)
+    w = W.WORKLOADS[args.prefill_workload]
+    if args.prefill_m:
+        w = w.with_(m=args.prefill_m)
+    d = stage_layer(w, 0, device=dev, experts_on_gpu=True, bulk_on_gpu=True, slots=args.resident_experts)
+    cfg = Q.make_cfg(w.dim, w.inter, w.n_routed, w.topk, w.gate_temp, w.norm_topk_prob, w.route_scale,
+                     w.swiglu_limit, max_tokens=w.m)
+    ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    Q.moe_v41_workspace_init(ws)
+    out = torch.empty((w.m, w.dim), dtype=torch.float32, device=dev)
+    tw = torch.empty((w.m, w.topk), dtype=torch.float32, device=dev)
+    ti = torch.empty((w.m, w.topk), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(x):
+        Q.moe_v41_forward(cfg, x, w.m, d.router_w, d.bias, d.expert_ptrs, w.shared_kind, d.sh1, d.sh3, d.sh2, out,
+                          tw, ti, None, ws, stream)
+
+    for _ in range(3):
+        call(d.x)
+    st = Q.moe_v41_read_status(ws, stream, clear=True)
+    if st:
+        raise RuntimeError(f"device status {st} during prefill warm-up")
+    distinct = float(np.unique(ti.cpu().numpy()).size)
+    K = args.prefill_steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    torch.cuda.synchronize()
+    clocks = Clocks(local_rank)
+    clocks.start()
+    for k in range(K):
+        evs[k].record(stream)
+        call(d.x)
+    evs[K].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    per_call = [evs[k].elapsed_time(evs[k + 1]) for k in range(K)]
+    st = Q.moe_v41_read_status(ws, stream, clear=True)
+    if st:
+        raise RuntimeError(f"device status {st} during the prefill timed region")
+    e2e = None
+    if not args.no_e2e:
+        xh = d.x.cpu().pin_memory()
+        oh = torch.empty((w.m, w.dim), dtype=torch.float32).pin_memory()
+        xd = torch.empty_like(d.x)
+
+        def e2e_call():
+            xd.copy_(xh, non_blocking=True)
+            call(xd)
+            oh.copy_(out, non_blocking=True)
+        for _ in range(2):
+            e2e_call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e = dict(ms=e0.elapsed_time(e1), steps=K, h2d=w.m * w.dim * 2, d2h=w.m * w.dim * 4)
+    launches = Q.moe_v41_kernel_launches(cfg, w.m, w.shared_kind)
+    return dict(w=w, K=K, per_call_ms=statistics.fmean(per_call), per_call_min_ms=min(per_call), distinct=distinct,
+                clocks=clk, e2e=e2e, launches_per_call=launches)
 
 
 def stage_x(w, l, dev):
@@ -313,9 +460,9 @@ def main():
             return
         K, Wm = args.steps, args.warmup
         cpu_baseline(w, L, max(1, min(Wm, ncores)), ncores)  # warm-up units
-        tps, dt, desc = cpu_baseline(w, L, K, ncores)
+        tps, dt, n, desc = cpu_baseline(w, L, K, ncores)
         line = {"impl": "reference", "metric": metric_name(w), "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": K, "warmup": Wm, "ms_per_step": dt * 1000.0 / K * ncores, "higher_is_better": True,
+                "steps": K, "warmup": Wm, "ms_per_step": 1000.0 / tps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": config_of(w, L, None),
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
@@ -328,6 +475,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     r = run_ours(args, rank, world, local_rank)
+    pf = None if args.no_prefill else run_prefill(args, local_rank)
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -337,19 +485,13 @@ def main():
     sec = r["ms"] / 1000.0
     tokens = world * w.m * K  # each step moves m tokens through all L layers, per GPU
     value = tokens / sec
-    hbm, kind = peaks()
-    bytes_call = algorithmic_bytes(w, r["distinct"])
-    achieved = bytes_call / (r["per_call_ms"] / 1000.0) / 1e9
     traffic = recorded_traffic(args.workload)
     line = {
         "metric": metric_name(w), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": r["ms"] / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8-dp4a/bf16-fma, f32 accumulate", "data": "synthetic",
         "config": config_of(w, L, r),
-        "roofline": {"bound": "hbm", "kernel": r["kernel"],
-                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_kind": kind, "traffic": traffic, "algorithmic_bytes_per_call": bytes_call,
-                     "us_per_call": r["per_call_ms"] * 1000.0, "frac_of_8tbs": achieved / 8000.0},
+        "roofline": roofline(w, r["distinct"], r["per_call_ms"], r["kernel"], traffic),
         "gpu_launches": (r["launches_per_call"] or 0) * L * K,
         "clocks": r["clocks"],
     }
@@ -358,10 +500,30 @@ def main():
         line["e2e"] = {"value": world * w.m * e["steps"] / (e["ms"] / 1000.0), "unit": "tokens/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
     if world == 1 and not args.no_cpu_baseline:
-        n_units = min(ncores, L * w.m)
-        tps, dt, desc = cpu_baseline(w, L, n_units, ncores)
+        tps, dt, n, desc = cpu_baseline(w, L, ncores, ncores, target_s=12.0)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
                                 "sample": desc + f", {dt:.1f} s"}
+    if pf:
+        pw = pf["w"]
+        sec = pf["per_call_ms"] / 1000.0
+        p = {"workload": pw.name, "metric": metric_name(pw), "value": world * pw.m / sec, "unit": "tokens/s",
+             "steps": pf["K"], "warmup": 3, "ms_per_step": pf["per_call_ms"], "ms_per_step_min": pf["per_call_min_ms"],
+             "config": config_of(pw, 1, {"distinct": pf["distinct"], "resident": 1, "rotated": False,
+                                         "resident_experts": args.resident_experts}),
+             "roofline": roofline(pw, pf["distinct"], pf["per_call_ms"],
+                                  f"the prefill kernels of one layer call ({pf['launches_per_call']} launches)",
+                                  recorded_traffic(pw.name)),
+             "gpu_launches": pf["launches_per_call"] * pf["K"], "clocks": pf["clocks"],
+             "dtype": "fp16 tensor-core GEMMs (gate/up split hi+lo), bf16 router/shared, f32 accumulate"}
+        if pf["e2e"]:
+            e = pf["e2e"]
+            p["e2e"] = {"value": world * pw.m * e["steps"] / (e["ms"] / 1000.0), "unit": "tokens/s",
+                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+        if world == 1 and not args.no_cpu_baseline:
+            tps, dt, n, desc = cpu_baseline(pw, 1, ncores, ncores, target_s=10.0)
+            p["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
+                                 "sample": desc + f", {dt:.1f} s"}
+        line["prefill"] = p
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

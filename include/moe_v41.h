@@ -85,8 +85,10 @@ enum {
   MOE_STATUS_TIMEOUT = 4u           /* an in-kernel wait exceeded wait_timeout_us; outputs are invalid */
 };
 
-/* Bytes of workspace a configuration needs (for up to cfg->max_tokens tokens).
- * Returns 0 for an invalid configuration. */
+/* Bytes of workspace a configuration needs (for up to cfg->max_tokens tokens;
+ * it includes the prefill kernels' buffers when cfg->path is MOE_PATH_PREFILL,
+ * or MOE_PATH_AUTO with max_tokens > 8).  Returns 0 for an invalid
+ * configuration. */
 MOE_API size_t moe_v41_workspace_bytes(const moe_v41_cfg* cfg);
 
 /* Prepare a workspace for first use: clears its control block and status word
@@ -117,7 +119,11 @@ MOE_API int moe_v41_route(const moe_v41_cfg* cfg, const void* x, int m, const vo
                   float* logits_out, float* topk_w, int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream);
 
 /* One MoE layer forward for m tokens (the metrale MoeV41::forward call, all
- * experts resident):
+ * experts resident).  Up to eight tokens run the decode kernels (one
+ * persistent launch of integer-dot GEMVs); above that, or with
+ * MOE_PATH_PREFILL, the prefill kernels (tokens grouped by expert, tensor-core
+ * GEMMs on dequantised tiles; router logits then carry the tensor cores' f32
+ * accumulation order).
  *   x           bf16 [m, dim], 16-B aligned
  *   router_w    bf16 [n_routed, dim], 16-B aligned
  *   bias        f32 [n_routed]
@@ -168,6 +174,10 @@ MOE_API int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, int m
                                     const void* sh_w1, const void* sh_w3, const void* sh_w2, float* out,
                                     float* topk_w, int32_t* topk_idx, float* logits_out, uint32_t* status_out,
                                     void* stream);
+
+/* Kernel launches one moe_v41_forward call with these arguments makes (for
+ * launch accounting and graph capture sizing); -1 for invalid arguments. */
+MOE_API int moe_v41_kernel_launches(const moe_v41_cfg* cfg, int m, int shared_kind);
 
 /* Synchronise `stream`, then copy the workspace status word (MOE_STATUS_* bits
  * accumulated since the last clear) to *status (host memory); clear == non-zero

@@ -51,6 +51,8 @@ def lib():
         L.moe_v41_forward.argtypes = [cfgp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.moe_v41_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32), i32]
         L.moe_v41_forward_noalloc.argtypes = [cfgp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_v41_kernel_launches.argtypes = [cfgp, i32, i32]
+        L.moe_v41_kernel_launches.restype = i32
         L.moe_v41_strerror.restype = ctypes.c_char_p
         L.moe_v41_strerror.argtypes = [i32]
         for f in ("moe_v41_workspace_init", "moe_v41_quantize_q8_1", "moe_v41_select_from_logits", "moe_v41_route",
@@ -139,6 +141,10 @@ def moe_v41_forward_noalloc(cfg, x, m, router_w, bias, expert_ptrs, shared_kind,
                                          shared_kind, _p(sh_w1), _p(sh_w3), _p(sh_w2), _p(out), _p(topk_w),
                                          _p(topk_idx), _p(logits_out), _p(status_out), _s(stream)),
            "moe_v41_forward_noalloc")
+
+
+def moe_v41_kernel_launches(cfg, m: int, shared_kind: int) -> int:
+    return int(lib().moe_v41_kernel_launches(ctypes.byref(cfg), int(m), int(shared_kind)))
 
 
 def moe_v41_read_status(ws, stream=None, clear: bool = False) -> int:

@@ -193,6 +193,13 @@ int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const void* ro
   return launch_decode_layer(dp, sms, s);
 }
 
+int moe_v41_kernel_launches(const moe_v41_cfg* cfg, int m, int shared_kind) {
+  if (check_cfg(cfg) != MOE_OK || m < 1 || m > cfg->max_tokens) return -1;
+  if (shared_kind != MOE_SHARED_BF16 && shared_kind != MOE_SHARED_KQUANT) return -1;
+  if (use_decode(cfg, m)) return m <= DECODE_MAX_M ? 1 : -1;
+  return prefill_possible(*cfg) ? prefill_launches(shared_kind) : -1;
+}
+
 int moe_v41_read_status(void* ws, void* stream, uint32_t* status, int clear) {
   if (!ws || !status) return MOE_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;

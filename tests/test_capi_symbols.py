@@ -22,7 +22,9 @@ def _declared():
 def lib():
     import quantized_mixture_experts_router_gb300 as Q
     import quantized_mixture_experts_router_gb300.build as qb
-    if not os.path.exists(Q.SO):
+    srcs = glob.glob(os.path.join(ROOT, "quantized_mixture_experts_router_gb300", "csrc", "*"))
+    srcs += glob.glob(os.path.join(ROOT, "include", "*.h"))
+    if not os.path.exists(Q.SO) or max(os.path.getmtime(f) for f in srcs) > os.path.getmtime(Q.SO):
         qb.build()
     return ctypes.CDLL(Q.SO)
 
@@ -48,3 +50,25 @@ def test_workspace_sizing_is_host_only(lib):
     assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 4, 6)) == 0        # topk above n_routed
     assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, gate_temp=0.0)) == 0
     assert Q.strerror(Q.MOE_ERR_WORKSPACE).startswith("workspace")
+
+
+def test_workspace_holds_prefill_buffers_only_when_prefill_can_run(lib):
+    import quantized_mixture_experts_router_gb300 as Q
+    dec = Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, max_tokens=8))
+    auto = Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, max_tokens=4096))
+    pre8 = Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, max_tokens=8, path=Q.MOE_PATH_PREFILL))
+    # 4096 tokens: at least the fp16 high/low activations, h and the per-pair expert outputs
+    assert auto > 4096 * 5120 * 4 + 4096 * 7 * (2304 * 2 + 5120 * 4)
+    assert pre8 > dec
+
+
+def test_kernel_launch_counts(lib):
+    import quantized_mixture_experts_router_gb300 as Q
+    auto = Q.make_cfg(5120, 2304, 384, 6, max_tokens=4096)
+    assert Q.moe_v41_kernel_launches(auto, 1, Q.MOE_SHARED_BF16) == 1       # one persistent decode kernel
+    assert Q.moe_v41_kernel_launches(auto, 8, Q.MOE_SHARED_KQUANT) == 1
+    assert Q.moe_v41_kernel_launches(auto, 9, Q.MOE_SHARED_BF16) == 11      # prefill, bf16 shared expert
+    assert Q.moe_v41_kernel_launches(auto, 4096, Q.MOE_SHARED_KQUANT) == 9  # shared expert as one more expert
+    assert Q.moe_v41_kernel_launches(auto, 4097, Q.MOE_SHARED_BF16) == -1
+    dec = Q.make_cfg(5120, 2304, 384, 6, max_tokens=16, path=Q.MOE_PATH_DECODE)
+    assert Q.moe_v41_kernel_launches(dec, 9, Q.MOE_SHARED_BF16) == -1
