@@ -60,7 +60,7 @@ constexpr int PF_GCH = 64;
 
 // Byte offsets of the prefill regions, relative to the prefill base.
 struct PrefillLayout {
-  size_t x16h, x16l, chunk, offsets, expert_ok, pair_tok, pair_w, pos_of, pos_sh, n_tiles, gu_tiles, dn_tiles, h16,
+  size_t xgh, xgl, chunk, offsets, expert_ok, pair_tok, pair_w, pos_of, pos_sh, n_tiles, gu_tiles, dn_tiles, h16,
       ep, hs, sp, total;
   size_t max_gu_tiles, max_dn_tiles;  // bounds on the column tiles over all experts
 };
@@ -85,8 +85,8 @@ inline PrefillLayout prefill_layout(const moe_v41_cfg& c) {
   const size_t nch = (T + PF_GCH - 1) / PF_GCH;
   L.max_gu_tiles = NE + V / PF_TN_GU + 1;
   L.max_dn_tiles = NE + V / PF_TN + 1;
-  L.x16h = take(T * c.dim * 2);
-  L.x16l = take(T * c.dim * 2);
+  L.xgh = take(V * c.dim * 2);
+  L.xgl = take(V * c.dim * 2);
   L.chunk = take(nch * NE * 4);
   L.offsets = take((NE + 1) * 4);
   L.expert_ok = take(NE * 4);
@@ -208,8 +208,9 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // status bit once) when the wait ran past the deadline.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t deadline,
                                                   unsigned* status) {
+  uint32_t tries = 0;
   while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
-    if (globaltimer_ns() > deadline) {
+    if ((++tries & 3u) == 0 && globaltimer_ns() > deadline) {
       atomicOr(status, (unsigned)MOE_STATUS_TIMEOUT);
       return false;
     }

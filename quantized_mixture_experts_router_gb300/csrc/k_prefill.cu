@@ -1,17 +1,18 @@
 // Prefill path (any m; taken by default above eight tokens): the expert
 // projections as GEMMs on the 5th-generation tensor cores.
 //
-//   x16     the q8_1 activation values fp16(d) * q (the values the method's
-//           integer dots stand for) as a high and a low fp16 part, exact
 //   router  logits = x W_R^T (bf16 tensor-core GEMM, f32 accumulation), then
 //           the selection per token
 //   group   (expert, token) pairs ordered by expert id, tokens ascending
 //           within an expert: the per-expert token lists of DeepSeek V4.1
 //           atlas "Mixture of experts" (model.py MoE.forward), made
 //           deterministic by a counting sort over token chunks
+//   xg      the q8_1 activation values fp16(d) * q (the values the method's
+//           integer dots stand for) as exact fp16 high + low parts, written
+//           in pair order
 //   gate/up per (expert, 128 rows, <= 128 pairs) tile: W1 and W3 rows
 //           dequantised from Q2_K, split into high and low fp16 parts, times
-//           the pairs' x16 rows (three products: hi.hi + hi.lo + lo.hi, about
+//           the pairs' xg rows (three products: hi.hi + hi.lo + lo.hi, about
 //           2^-22 relative); the epilogue applies the clipped SwiGLU,
 //           quantises h to q8_1 and stores fp16 of its values.  The split is
 //           needed because q8_1(h) turns any error in h near a rounding
@@ -23,14 +24,17 @@
 //   combine out = sum over the token's experts in ascending id of G_i E_i,
 //           then the shared expert's output added last
 //
-// GEMM block (128 weight rows x up to 128 or 256 columns): eight producer
-// warps fill a ring of 128-byte-swizzled K-major tiles (dequantising K-quant
-// blocks on the way, two threads per weight row), one thread issues
+// GEMM block (128 weight rows x up to 128 or 256 columns): a TMA thread loads
+// the B rows (and bf16 A rows) of each K chunk into 128-byte-swizzled K-major
+// stage tiles; for K-quant A, sixteen producer warps dequantise staged raw
+// blocks into the A tiles (four threads per weight row, one 16-value
+// sub-block each, through per-sub-block lookup tables); one thread issues
 // tcgen05.mma (M = 128, N = tile width, K = 16) into a tensor-memory
-// accumulator and commits each stage back to the producers, and the same
-// eight warps then read the accumulator for the epilogue.  Products
-// accumulate in f32; bf16 operands (router, bf16 shared expert) are the
-// caller's values, exact.
+// accumulator and commits each stage back; the producer warps then read the
+// accumulator for the epilogue.  Products accumulate in f32; bf16 operands
+// (router, bf16 shared expert) are the caller's values, exact.
+#include <cudaTypedefs.h>
+
 #include "internal.h"
 #include "tc.cuh"
 
@@ -40,8 +44,6 @@ namespace {
 
 constexpr int TM = PF_TM;
 constexpr int KC = PF_KC;
-constexpr int NPROD = 256;   // producer / epilogue threads (8 warps); one more warp issues the MMAs
-constexpr int GTHREADS = NPROD + 32;
 
 enum : int { A_BF16 = 0, A_Q2K = 1, A_Q3K = 2 };
 enum : int { E_F32 = 0, E_SWIGLU_Q8 = 1, E_SWIGLU_BF16 = 2 };
@@ -50,12 +52,16 @@ __device__ __forceinline__ uint32_t f2h(float v) { return (uint32_t)__half_as_us
 
 // ------------------------------------------------------------------ prep
 // The q8_1 values of x, fp16(d) * q (exact in f32), as fp16 high and low
-// parts; one thread per block of 32 (the q8_1 rule: d = amax / 127,
-// q = round-half-away(v / d), d stored as fp16).
-__global__ void k_x16(const uint16_t* __restrict__ x, int m, int D, uint16_t* __restrict__ x16h,
-                      uint16_t* __restrict__ x16l) {
-  const long nb = (long)m * (D / 32);
+// parts, written to the row of every (expert, token) pair of the token (and
+// of the K-quant shared expert's pair), so the gate/up GEMM reads its B
+// operand as contiguous rows.  One thread per block of 32 (the q8_1 rule:
+// d = amax / 127, q = round-half-away(v / d), d stored as fp16).
+__global__ void k_xg(const uint16_t* __restrict__ x, int m, int D, int k, const int* __restrict__ pos_of,
+                     const int* __restrict__ pos_sh, uint16_t* __restrict__ xgh, uint16_t* __restrict__ xgl) {
+  const int nq = D / 32;
+  const long nb = (long)m * nq;
   for (long g = blockIdx.x * (long)blockDim.x + threadIdx.x; g < nb; g += (long)gridDim.x * blockDim.x) {
+    const int t = (int)(g / nq), qb = (int)(g % nq);
     const uint4* xp = reinterpret_cast<const uint4*>(x + g * 32);
     uint32_t raw[16];
 #pragma unroll
@@ -81,12 +87,16 @@ __global__ void k_x16(const uint16_t* __restrict__ x, int m, int D, uint16_t* __
       oh[i] = *reinterpret_cast<const uint32_t*>(&hh);
       ol[i] = *reinterpret_cast<const uint32_t*>(&ll);
     }
-    uint4* ph = reinterpret_cast<uint4*>(x16h + g * 32);
-    uint4* pl = reinterpret_cast<uint4*>(x16l + g * 32);
+    for (int i = 0; i <= k; ++i) {
+      const int pos = i < k ? __ldg(pos_of + (size_t)t * k + i) : (pos_sh ? __ldg(pos_sh + t) : -1);
+      if (pos < 0) continue;
+      uint4* ph = reinterpret_cast<uint4*>(xgh + (size_t)pos * D + qb * 32);
+      uint4* pl = reinterpret_cast<uint4*>(xgl + (size_t)pos * D + qb * 32);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      ph[i] = make_uint4(oh[4 * i], oh[4 * i + 1], oh[4 * i + 2], oh[4 * i + 3]);
-      pl[i] = make_uint4(ol[4 * i], ol[4 * i + 1], ol[4 * i + 2], ol[4 * i + 3]);
+      for (int c = 0; c < 4; ++c) {
+        ph[c] = make_uint4(oh[4 * c], oh[4 * c + 1], oh[4 * c + 2], oh[4 * c + 3]);
+        pl[c] = make_uint4(ol[4 * c], ol[4 * c + 1], ol[4 * c + 2], ol[4 * c + 3]);
+      }
     }
   }
 }
@@ -280,18 +290,22 @@ __global__ void k_combine(const int* __restrict__ idx, const int* __restrict__ p
 }
 
 // ------------------------------------------------------------------ GEMM
+enum : int { B_TILED = 0, B_GATHER = 1 };
+constexpr int B_BOX = 16;  // rows per B box of the expert GEMMs: a tile loads only the rows it uses
+
 struct GemmArgs {
-  int K;                               // contraction length, a multiple of 64
+  CUtensorMap map_a[2];                // bf16 A matrices (box 64 x 128)
+  CUtensorMap map_b[2];                // B rows (high, low parts): box 64 x B_BOX (expert jobs), 64 x TNM
+                                       // (plain jobs) or 64 x 1 (gather)
+  int K;                               // contraction length: a multiple of 256 (K-quant A) or 64 (bf16 A)
   int a_rows;                          // rows of A (the M extent)
-  int a_row_bytes;                     // bytes per A row
-  const uint8_t* a0;                   // A matrices of a plain job, or of the pseudo-expert
+  int a_row_bytes;                     // K-quant A: bytes per row
+  const uint8_t* a0;                   // K-quant A of a plain job, or of the pseudo-expert
   const uint8_t* a1;
   const unsigned long long* eptr;      // expert jobs: the [N][3] pointer table
   int pj0, pj1;                        // pointer-table columns of the job's matrices
   int pseudo;                          // expert whose matrices are a0 / a1 (-1: none)
-  const uint16_t* b;                   // B rows of K values (the high parts when split)
-  const uint16_t* b_lo;                // split B: the low parts
-  const int* b_rows;                   // B row of each column, or null: the column itself
+  const int* b_rows;                   // gather: B row of each column
   int cols;                            // plain jobs: number of columns
   const int4* tiles;                   // expert jobs: (e, mt, nt) per block
   const int* n_tiles;
@@ -307,141 +321,99 @@ struct GemmArgs {
 
 constexpr uint32_t A_TILE = TM * 128;  // bytes of one A tile (128 rows x 64 values)
 
-template <int NS>
+// Raw K-quant staging.  A UNIT is the stretch of every tile row's blocks that
+// a group of consecutive K chunks reads: Q2_K half a super-block (2 chunks:
+// its 32 quant bytes, 8 scale bytes and d/dmin = 11 words), Q3_K a whole
+// super-block (4 chunks; the 4-byte-aligned window of 28 words over its 110
+// bytes, which are only 2-byte aligned).  Shared memory holds it row-major
+// with an odd pitch (11 or 29 words): the copies of one row's consecutive
+// words coalesce, and one word of 32 consecutive rows falls in 32 banks.
+template <int AK>
+struct RawGeo {
+  static constexpr int words() { return AK == A_Q2K ? 11 : 28; }
+  static constexpr int PITCH = AK == A_Q2K ? 11 : 29;
+  static constexpr uint32_t BYTES = AK == A_BF16 ? 0u : (uint32_t)(TM * PITCH * 4);  // one matrix, one buffer
+};
+
+template <int NSA, int NSB, int RAWN>
 struct GemmCtl {
-  unsigned long long full[NS], empty[NS], acc;
+  unsigned long long full_a[NSA], empty_a[NSA], full_b[NSB], empty_b[NSB], acc;
+  unsigned long long raw_full[RAWN], raw_free[RAWN];
   uint32_t tmem;
 };
 
-// Shared-memory plan of one GEMM variant: per stage NMAT A tiles (times two
-// when split into high and low fp16 parts), then one B tile (two when split)
-// of TNM rows.
-template <int NMAT, bool SPLIT, int TNM, int NS>
+// Memory plan of one GEMM variant.  A ring of NSA A stages (NMAT A tiles
+// each, times two when split into high and low fp16 parts): in tensor memory
+// for K-quant A (written by the dequantising threads, lane = row), in shared
+// memory for bf16 A (loaded by TMA together with B, in the A stage of the B
+// stage's index).  In shared memory: a ring of NSB B stages (one B tile of
+// TNM rows, two when split), RAWN raw buffers per matrix for K-quant A, the
+// control block and the gathered B row indices.
+template <int AK, int NMAT, bool SPLIT, int TNM, int NSA, int NSB, int RAWN>
 struct Plan {
   static constexpr int NPART = SPLIT ? 2 : 1;
   static constexpr uint32_t B_TILE = TNM * 128;
-  static constexpr uint32_t STAGE = NMAT * NPART * A_TILE + NPART * B_TILE;
-  static constexpr size_t SMEM = 1024 + (size_t)NS * STAGE + sizeof(GemmCtl<NS>);
-  static __device__ __forceinline__ uint32_t a_off(int mat, int part) { return (mat * NPART + part) * A_TILE; }
-  static __device__ __forceinline__ uint32_t b_off(int part) { return NMAT * NPART * A_TILE + part * B_TILE; }
+  static constexpr uint32_t A_STAGE = NMAT * NPART * A_TILE;
+  static constexpr uint32_t B_STAGE = NPART * B_TILE;
+  static constexpr bool ATMEM = AK != A_BF16;  // K-quant A lives in tensor memory
+  static constexpr uint32_t B_RING = ATMEM ? 0u : NSA * A_STAGE;
+  // tensor-memory columns: accumulators [0, 256), K-quant A stages from 256
+  static constexpr uint32_t TA_COLS = NMAT * NPART * 32;  // columns of one A stage (64 K values per tile)
+  static_assert(!ATMEM || 256 + NSA * TA_COLS <= 512, "A stages exceed tensor memory");
+  static constexpr uint32_t RAW_OFF = B_RING + NSB * B_STAGE;
+  static constexpr uint32_t RAW = RAWN * NMAT * RawGeo<AK>::BYTES;
+  static constexpr uint32_t CTL = RAW_OFF + RAW;
+  static constexpr uint32_t ROWS = CTL + ((sizeof(GemmCtl<NSA, NSB, RAWN>) + 15) & ~15);
+  static constexpr size_t SMEM = 1024 + (size_t)ROWS + TNM * 4;
+  static __device__ __forceinline__ uint32_t a_off(int sa, int mat, int part) {
+    return sa * A_STAGE + (mat * NPART + part) * A_TILE;
+  }
+  static __device__ __forceinline__ uint32_t b_off(int sb, int part) { return B_RING + sb * B_STAGE + part * B_TILE; }
+  static __device__ __forceinline__ uint32_t raw_off(int mat, int buf) {
+    return RAW_OFF + (buf * NMAT + mat) * RawGeo<AK>::BYTES;
+  }
 };
 
-// 32-bit word at a 2-byte aligned address p, from the two aligned words
-// around it (reads the 8 bytes [p & ~3, (p & ~3) + 8))
-__device__ __forceinline__ uint32_t ldg_u32_a2(const uint8_t* p) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* base = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-  return __funnelshift_r(__ldg(base), __ldg(base + 1), (uint32_t)(a & 3u) * 8u);
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// the same from two 16-bit loads (reads exactly [p, p + 4))
-__device__ __forceinline__ uint32_t ldg_u32_a2_exact(const uint8_t* p) {
-  const unsigned short* h = reinterpret_cast<const unsigned short*>(p);
-  return (uint32_t)__ldg(h) | ((uint32_t)__ldg(h + 1) << 16);
+// arrive (without a pending-count increment) on the mbarrier once every
+// cp.async this thread has issued so far has landed
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// eight f32 values as fp16 into a 16-byte tile chunk; when split, the
-// residual v - fp16(v) as fp16 into the same chunk of the low tile
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Lookup tables of one Q2_K sub-block: w(q) = d sc q - dmin mn for q = 0..3
+// as fp16 high parts (hi01 = w0 | w1 << 16, hi23 = w2 | w3 << 16) and, when
+// split, the fp16 residuals w(q) - hi(q).
 template <bool SPLIT>
-__device__ __forceinline__ void emit8(const float* v, uint8_t* hi, uint8_t* lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __half2 hh = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
-    h[e] = *reinterpret_cast<const uint32_t*>(&hh);
-    if constexpr (SPLIT) {
-      const float2 back = __half22float2(hh);
-      const __half2 ll = __floats2half2_rn(v[2 * e] - back.x, v[2 * e + 1] - back.y);
-      l[e] = *reinterpret_cast<const uint32_t*>(&ll);
-    }
+__device__ __forceinline__ void q2k_tables(float d, float dmin, uint32_t scbyte, uint32_t& hi01, uint32_t& hi23,
+                                           uint32_t& lo01, uint32_t& lo23) {
+  const float A = d * (float)(scbyte & 15u), B = dmin * (float)(scbyte >> 4);
+  const float w0 = -B, w1 = A - B, w2 = fmaf(2.0f, A, -B), w3 = fmaf(3.0f, A, -B);
+  const __half2 ha = __floats2half2_rn(w0, w1), hb = __floats2half2_rn(w2, w3);
+  hi01 = h2bits(ha);
+  hi23 = h2bits(hb);
+  if constexpr (SPLIT) {
+    const float2 fa = __half22float2(ha), fb = __half22float2(hb);
+    lo01 = h2bits(__floats2half2_rn(w0 - fa.x, w1 - fa.y));
+    lo23 = h2bits(__floats2half2_rn(w2 - fb.x, w3 - fb.y));
   }
-  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
-  if constexpr (SPLIT) *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Half hf (K values 32 hf .. 32 hf + 31) of chunk kc of one A row into row r
-// of the swizzled tile(s): 16-byte chunks 4 hf .. 4 hf + 3.
-template <int AK, bool SPLIT>
-__device__ __forceinline__ void produce_a(const uint8_t* row, int kc, int hf, uint8_t* hi, uint8_t* lo, int r) {
-  if constexpr (AK == A_BF16) {
-    const uint4* src = reinterpret_cast<const uint4*>(row + (size_t)kc * 128) + 4 * hf;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(hi + swz(r, 4 * hf + c)) = __ldg(src + c);
-  } else if constexpr (AK == A_Q2K) {
-    // GGUF Q2_K super-block: scales[16] (low nibble scale, high nibble min),
-    // qs[64] (2-bit planes), fp16 d, dmin.  Element 128h + 32j + l (l < 32)
-    // is bits 2j of qs[32h + l], in sub-block 8h + 2j + (l >= 16):
-    // d * sc * q - dmin * mn.  Chunk kc is quarter (kc & 3) of super-block
-    // kc / 4: half h = (kc & 3) / 2, planes j0 = 2 (kc & 1) and j0 + 1; this
-    // thread's half of it is plane j = j0 + hf.
-    const uint8_t* blk = row + (size_t)(kc >> 2) * Q2K_B;
-    const int part = kc & 3, h = part >> 1, j0 = 2 * (part & 1), j = j0 + hf;
-    const uint32_t* bw = reinterpret_cast<const uint32_t*>(blk);
-    uint32_t qs[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) qs[i] = __ldg(bw + 4 + 8 * h + i);
-    const uint32_t sc = __ldg(bw + 2 * h + (j0 >> 1));  // scale bytes of sub-blocks 8h + 2j0 .. + 3
-    const uint32_t dd = __ldg(bw + 20);
-    const float d = half_bits_to_float(dd), dmin = half_bits_to_float(dd >> 16);
-    float am[2], bm[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {  // sub-blocks 8h + 2j + u
-      const uint32_t byte = (sc >> (8 * (2 * hf + u))) & 0xFFu;
-      am[u] = d * (float)(byte & 15u);
-      bm[u] = dmin * (float)(byte >> 4);
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {  // l = 8c .. 8c + 7
-      const int u = c >> 1;
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int l = 8 * c + e;
-        const float q = (float)((qs[l >> 2] >> (8 * (l & 3) + 2 * j)) & 3u);
-        v[e] = fmaf(am[u], q, -bm[u]);
-      }
-      emit8<SPLIT>(v, hi + swz(r, 4 * hf + c), lo + swz(r, 4 * hf + c));
-    }
-  } else {
-    // GGUF Q3_K super-block (110 bytes, 2-byte aligned): hmask[32], qs[64],
-    // scales[12] (sixteen 6-bit codes: low nibbles in bytes 0-7, high bit
-    // pairs in bytes 8-11), fp16 d.  Element 128h + 32j + l is
-    // (bits 2j of qs[32h + l]) + 4 * (bit 4h + j of hmask[l]) - 4, times
-    // d * (code - 32) of sub-block 8h + 2j + (l >= 16).
-    const uint8_t* blk = row + (size_t)(kc >> 2) * Q3K_B;
-    const int part = kc & 3, h = part >> 1, j = 2 * (part & 1) + hf;
-    uint32_t qs[8], hm[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      qs[i] = ldg_u32_a2(blk + 32 + 32 * h + 4 * i);
-      hm[i] = ldg_u32_a2(blk + 4 * i);
-    }
-    const uint32_t s_lo = ldg_u32_a2(blk + 96 + 4 * (j >> 1));  // low-nibble bytes 2j, 2j + 1
-    const uint32_t s_hi = ldg_u32_a2_exact(blk + 104);           // the block's last bytes: no read past it
-    const float d = half_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(blk + 108)));
-    float am[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int sb = 2 * j + u;  // sub-block index mod 8
-      const uint32_t lo4 = (s_lo >> (8 * (sb & 3) + 4 * h)) & 15u;
-      const uint32_t hi2 = (s_hi >> (8 * (sb & 3) + 2 * (2 * h + (j >> 1)))) & 3u;
-      am[u] = d * (float)((int)(lo4 | (hi2 << 4)) - 32);
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int u = c >> 1;
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int l = 8 * c + e;
-        const uint32_t q = (qs[l >> 2] >> (8 * (l & 3) + 2 * j)) & 3u;
-        const uint32_t hb = (hm[l >> 2] >> (8 * (l & 3) + 4 * h + j)) & 1u;
-        v[e] = am[u] * (float)((int)(q | (hb << 2)) - 4);
-      }
-      emit8<SPLIT>(v, hi + swz(r, 4 * hf + c), lo + swz(r, 4 * hf + c));
-    }
-  }
-}
+// PRMT selectors of two table entries: the 2-bit codes q0, q1 in bytes 0, 1
+// of qq select bytes (2q0, 2q0+1, 2q1, 2q1+1) of the 8-byte table.
+__device__ __forceinline__ uint32_t pair_sel(uint32_t qq) { return qq * 0x22u + 0x1010u; }
 
 // q8_1 of one 32-value block of h held one value per lane: fp16 bits of
 // fp16(d) * q for this lane's value
@@ -456,20 +428,39 @@ __device__ __forceinline__ uint16_t q8_h16_warp(float v) {
 }
 
 // One tile: D[128 rows, TN columns] (per matrix) = A . B^T over K.
+//   warps 0 .. NPW-1       K-quant A: dequantise staged raw blocks into the
+//                          A ring; then the epilogue (all variants)
+//   next NLW warps         K-quant A: copy the raw blocks of each unit into
+//                          the raw ring (asynchronous copies; these warps never
+//                          fence, so no copy in flight delays a stage hand-over)
+//   next warp              lane 0: TMA loads of B (and of bf16 A) per stage
+//   last warp              lane 0: tcgen05.mma issue
 // SPLIT: A = A_hi + A_lo and B = B_hi + B_lo in fp16, accumulating
 // A_hi B_hi + A_hi B_lo + A_lo B_hi (the A_lo B_lo term is below 2^-22
 // relative).
-template <int AK, int NMAT, bool SPLIT, int EPI, int TNM, int NS>
-__global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ GemmArgs g) {
-  using PL = Plan<NMAT, SPLIT, TNM, NS>;
+template <int AK>
+constexpr int loader_warps() { return AK == A_BF16 ? 0 : 4; }
+
+template <int AK, int NMAT, bool SPLIT, int EPI, int TNM, int NSA, int NSB, int RAWN, int NPROD, int BMODE>
+__global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gemm(const __grid_constant__ GemmArgs g) {
+  using PL = Plan<AK, NMAT, SPLIT, TNM, NSA, NSB, RAWN>;
+  using RG = RawGeo<AK>;
+  constexpr bool KQ = AK != A_BF16;
+  static_assert(KQ || NSA == NSB, "bf16 A shares the B stage index");
+  static_assert(!KQ || NPROD == 4 * TM, "the K-quant producers take one 16-value sub-block each");
+  constexpr int NPW = NPROD / 32;       // producer warps
+  constexpr int NLW = loader_warps<AK>();  // raw loader warps
   extern __shared__ __align__(1024) uint8_t raw_smem[];
   uint8_t* sm = raw_smem + ((1024u - (smem_u32(raw_smem) & 1023u)) & 1023u);
-  GemmCtl<NS>& C = *reinterpret_cast<GemmCtl<NS>*>(sm + NS * PL::STAGE);
+  GemmCtl<NSA, NSB, RAWN>& C = *reinterpret_cast<GemmCtl<NSA, NSB, RAWN>*>(sm + PL::CTL);
+  int* s_rows = reinterpret_cast<int*>(sm + PL::ROWS);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int W_LOAD = NPW, W_TMA = NPW + NLW, W_MMA = NPW + NLW + 1;
+  auto B = [](unsigned long long& b) { return reinterpret_cast<uint64_t*>(&b); };
 
   // ---- the tile of this block (block-uniform)
   int mt, col0, ncol;
-  const uint8_t *A0, *A1 = nullptr;
+  const uint8_t *A0 = nullptr, *A1 = nullptr;
   if (g.tiles) {
     if ((int)blockIdx.x >= __ldg(g.n_tiles)) return;
     const int4 t = __ldg(g.tiles + blockIdx.x);
@@ -481,7 +472,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
     if (e == g.pseudo) {
       A0 = g.a0;
       A1 = g.a1;
-    } else {
+    } else if (KQ) {
       A0 = reinterpret_cast<const uint8_t*>(__ldg(g.eptr + (size_t)e * 3 + g.pj0));
       if (NMAT == 2) A1 = reinterpret_cast<const uint8_t*>(__ldg(g.eptr + (size_t)e * 3 + g.pj1));
     }
@@ -496,17 +487,31 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
   const int TN = (ncol + 15) & ~15;  // MMA width: a multiple of 16, <= TNM
   uint32_t ncols_tmem = 32;
   while (ncols_tmem < (uint32_t)(NMAT * TN)) ncols_tmem <<= 1;
+  if (PL::ATMEM) ncols_tmem = 512;
   const int row0 = mt * TM;
   const int nk = g.K / KC;
   const uint64_t deadline = globaltimer_ns() + g.timeout_ns;
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(reinterpret_cast<uint64_t*>(&C.full[s]), NPROD);
-      mbar_init(reinterpret_cast<uint64_t*>(&C.empty[s]), 1);
+    for (int s = 0; s < NSA; ++s) {
+      mbar_init(B(C.full_a[s]), NPROD);
+      mbar_init(B(C.empty_a[s]), 1);
     }
-    mbar_init(reinterpret_cast<uint64_t*>(&C.acc), 1);
+    for (int s = 0; s < NSB; ++s) {
+      mbar_init(B(C.full_b[s]), 1);
+      mbar_init(B(C.empty_b[s]), 1);
+    }
+    mbar_init(B(C.acc), 1);
+    if constexpr (KQ) {
+      for (int b = 0; b < RAWN; ++b) {
+        mbar_init(B(C.raw_full[b]), NLW * 32);
+        mbar_init(B(C.raw_free[b]), NPROD);
+      }
+    }
     fence_mbar_init();
+  }
+  if (BMODE == B_GATHER && warp == W_TMA) {
+    for (int i = lane; i < TN; i += 32) s_rows[i] = __ldg(g.b_rows + col0 + min(i, ncol - 1));
   }
   if (warp == 0) tmem_alloc(&C.tmem, ncols_tmem);
   tc_fence_before();
@@ -514,58 +519,170 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
   tc_fence_after();
   const uint32_t tmem = C.tmem;
 
-  if (warp < NPROD / 32) {
+  if (warp < NPW) {
     // ------------------------------------------------------ producers
-    const int r = tid & (TM - 1), hf = tid >> 7;  // A row, and which half of its 64 K values
-    const bool row_ok = row0 + r < g.a_rows;
-    const uint8_t* arow0 = A0 + (size_t)(row0 + r) * g.a_row_bytes;
-    const uint8_t* arow1 = NMAT == 2 ? A1 + (size_t)(row0 + r) * g.a_row_bytes : nullptr;
-    for (int kc = 0; kc < nk; ++kc) {
-      const int s = kc % NS;
-      if (kc >= NS && !mbar_wait_bounded(reinterpret_cast<uint64_t*>(&C.empty[s]), (uint32_t)((kc / NS - 1) & 1),
-                                         deadline, g.status))
-        break;
-      uint8_t* st = sm + (size_t)s * PL::STAGE;
-      if (row_ok) {
-        produce_a<AK, SPLIT>(arow0, kc, hf, st + PL::a_off(0, 0), st + PL::a_off(0, SPLIT ? 1 : 0), r);
-        if (NMAT == 2)
-          produce_a<AK, SPLIT>(arow1, kc, hf, st + PL::a_off(1, 0), st + PL::a_off(1, SPLIT ? 1 : 0), r);
-      } else {
+    const int r = tid & (TM - 1), qd = tid >> 7;  // A row; sub-block u = qd & 1 of plane half jj = qd >> 1
+    const int jj = qd >> 1, u = qd & 1;
+    bool ok = true;
+    if constexpr (KQ) {
+      const bool row_ok = row0 + r < g.a_rows;
+      const uint8_t* Am[2] = {A0, A1};
+      const uint32_t raw_base = smem_u32(sm);
+      const int nunits = nk / (AK == A_Q2K ? 2 : 4);  // K chunks per unit: 2 (Q2_K half block), 4 (Q3_K block)
+      // this thread's 8 TMEM columns of A stage sa, matrix m, part pt: the
+      // 16 K values 32 jj + 16 u .. + 15 of its row (lane = row)
+      const uint32_t ta_lane = tmem + 256u + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(16 * jj + 8 * u);
+      auto ta_addr = [&](int sa, int m, int pt) -> uint32_t {
+        return ta_lane + (uint32_t)(sa * PL::TA_COLS + (m * PL::NPART + pt) * 32);
+      };
+      // one K chunk: wait for the A stage, store this thread's piece, hand over
+      auto chunk = [&](int kc, auto&& fillA) -> bool {
+        const int sa = kc % NSA;
+        if (kc >= NSA && !mbar_wait_bounded(B(C.empty_a[sa]), (uint32_t)((kc / NSA - 1) & 1), deadline, g.status))
+          return false;
+        tc_fence_after();
+        if (row_ok) {
+          fillA(sa);
+        } else {
+          const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m)
+          for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-          for (int pt = 0; pt < PL::NPART; ++pt)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              *reinterpret_cast<uint4*>(st + PL::a_off(m, pt) + swz(r, 4 * hf + c)) = make_uint4(0, 0, 0, 0);
-      }
-      for (int q = tid; q < TN * 8; q += NPROD) {
-        const int col = q >> 3, c = q & 7;
-        uint4 v = make_uint4(0, 0, 0, 0), vl = make_uint4(0, 0, 0, 0);
-        if (col < ncol) {
-          const int brow = g.b_rows ? __ldg(g.b_rows + col0 + col) : col0 + col;
-          const size_t off = (size_t)brow * g.K + (size_t)kc * KC;
-          v = __ldg(reinterpret_cast<const uint4*>(g.b + off) + c);
-          if (SPLIT) vl = __ldg(reinterpret_cast<const uint4*>(g.b_lo + off) + c);
+            for (int pt = 0; pt < PL::NPART; ++pt) tmem_st8(ta_addr(sa, m, pt), z);
         }
-        *reinterpret_cast<uint4*>(st + PL::b_off(0) + swz(col, c)) = v;
-        if (SPLIT) *reinterpret_cast<uint4*>(st + PL::b_off(1) + swz(col, c)) = vl;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(B(C.full_a[sa]));
+        return true;
+      };
+      for (int v = 0; v < nunits && ok; ++v) {
+        const int buf = v % RAWN;
+        if (!mbar_wait_bounded(B(C.raw_full[buf]), (uint32_t)((v / RAWN) & 1), deadline, g.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t* rw[2];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) rw[m] = reinterpret_cast<const uint32_t*>(sm + PL::raw_off(m, buf)) + r * RG::PITCH;
+        if constexpr (AK == A_Q2K) {
+          // half h of super-block v / 2: chunks 2v, 2v + 1 (parts 2h, 2h + 1)
+          uint32_t qs[NMAT][4], sc[NMAT][2], dd[NMAT];
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qs[m][i] = rw[m][(4 * u + i)];
+            sc[m][0] = rw[m][8];
+            sc[m][1] = rw[m][9];
+            dd[m] = rw[m][10];
+          }
+#pragma unroll
+          for (int cp = 0; cp < 2 && ok; ++cp) {
+            const int j = 2 * cp + jj;  // this thread's 2-bit plane
+            ok = chunk(2 * v + cp, [&](int sa) {
+#pragma unroll
+              for (int m = 0; m < NMAT; ++m) {
+                const float d = half_bits_to_float(dd[m]), dmin = half_bits_to_float(dd[m] >> 16);
+                const int sbi = 2 * j + u;  // sub-block 8h + sbi: scale byte sbi of the half
+                const uint32_t byte = (sc[m][sbi >> 2] >> (8 * (sbi & 3))) & 0xFFu;
+                uint32_t th0, th1, tl0 = 0, tl1 = 0;
+                q2k_tables<SPLIT>(d, dmin, byte, th0, th1, tl0, tl1);
+                uint32_t oh[8], ol[8];  // values l = 16u .. 16u + 15 in pairs: qs words 0..3 of the sub-block
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                  const uint32_t qq = (qs[m][f] >> (2 * j)) & 0x03030303u;
+                  const uint32_t s0 = pair_sel(qq), s1 = pair_sel(qq >> 16);
+                  oh[2 * f] = prmt(th0, th1, s0);
+                  oh[2 * f + 1] = prmt(th0, th1, s1);
+                  if (SPLIT) {
+                    ol[2 * f] = prmt(tl0, tl1, s0);
+                    ol[2 * f + 1] = prmt(tl0, tl1, s1);
+                  }
+                }
+                tmem_st8(ta_addr(sa, m, 0), oh);
+                if (SPLIT) tmem_st8(ta_addr(sa, m, SPLIT ? 1 : 0), ol);
+              }
+            });
+          }
+        } else {
+          // Q3_K super-block v: the row's 110 bytes start o = 0 or 2 bytes
+          // into the staged window; block word i = window bytes 4i+o .. 4i+o+3
+          static_assert(NMAT == 1 && !SPLIT, "the Q3_K producer serves the single-matrix, unsplit GEMM");
+          const uint32_t o = (uint32_t)(reinterpret_cast<uintptr_t>(Am[0] + (size_t)(row0 + r) * g.a_row_bytes +
+                                                                     (size_t)v * Q3K_B) & 3u);
+          const uint32_t fsel = o ? 0x5432u : 0x3210u;
+          const uint32_t* wv = rw[0];
+          uint32_t hm[4], sc[3], dword;
+          {
+            uint32_t prev = wv[(4 * u)];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {  // block words 4u .. 4u + 3 (hmask bytes 16u .. 16u + 15)
+              const uint32_t nxt = wv[(4 * u + i + 1)];
+              hm[i] = prmt(prev, nxt, fsel);
+              prev = nxt;
+            }
+            prev = wv[24];
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {  // block words 24 .. 26 (scales)
+              const uint32_t nxt = wv[(25 + i)];
+              sc[i] = prmt(prev, nxt, fsel);
+              prev = nxt;
+            }
+            dword = o ? (prev >> 16) : (prev & 0xFFFFu);  // block bytes 108, 109 (prev = window word 27)
+          }
+          const float d = half_bits_to_float(dword);
+          const __half2 m1028 = bits2h(0xE404E404u);  // -1028 in both halves
+#pragma unroll
+          for (int hh = 0; hh < 2 && ok; ++hh) {
+            uint32_t qs[4];
+            {
+              uint32_t prev = wv[(8 + 8 * hh + 4 * u)];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {  // block words 8 + 8hh + 4u + i (qs bytes 32hh + 16u + 4i ..)
+                const uint32_t nxt = wv[(9 + 8 * hh + 4 * u + i)];
+                qs[i] = prmt(prev, nxt, fsel);
+                prev = nxt;
+              }
+            }
+#pragma unroll
+            for (int cp = 0; cp < 2 && ok; ++cp) {
+              const int j = 2 * cp + jj;
+              ok = chunk(4 * v + 2 * hh + cp, [&](int sa) {
+                const int sbi = 2 * j + u;  // sub-block 8hh + sbi
+                const uint32_t lo4 = (sc[sbi >> 2] >> (8 * (sbi & 3) + 4 * hh)) & 15u;
+                const uint32_t hi2 = (sc[2] >> (8 * (sbi & 3) + 2 * (2 * hh + (j >> 1)))) & 3u;
+                const __half2 ds = __float2half2_rn(d * (float)((int)(lo4 | (hi2 << 4)) - 32));
+                uint32_t oh[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const uint32_t lo2 = (qs[i] >> (2 * j)) & 0x03030303u;
+                  const uint32_t hb = (hm[i] >> (4 * hh + j)) & 0x01010101u;
+                  const uint32_t q = lo2 + hb * 4u;  // lo | hb << 2, per byte: 0..7
+                  // fp16 1024 + q per value, minus 1028 (exact: q - 4), times d (code - 32)
+                  oh[2 * i] = h2bits(__hmul2(__hadd2(bits2h(prmt(q, 0x64646464u, 0x4140u)), m1028), ds));
+                  oh[2 * i + 1] = h2bits(__hmul2(__hadd2(bits2h(prmt(q, 0x64646464u, 0x4342u)), m1028), ds));
+                }
+                tmem_st8(ta_addr(sa, 0, 0), oh);
+              });
+            }
+          }
+        }
+        // raw buffer `buf` is free once every producer has read it
+        mbar_arrive(B(C.raw_free[buf]));
       }
-      fence_async_smem();
-      mbar_arrive(reinterpret_cast<uint64_t*>(&C.full[s]));
     }
     // ------------------------------------------------------- epilogue
     // The MMA thread always commits the accumulator barrier (after its last
     // issued MMA), so a second bounded wait after a timeout still ends with
     // no MMA in flight before the tensor memory is read or freed.
-    if (lane == 0 && !mbar_wait_bounded(reinterpret_cast<uint64_t*>(&C.acc), 0u, deadline, g.status))
-      mbar_wait_bounded(reinterpret_cast<uint64_t*>(&C.acc), 0u, globaltimer_ns() + g.timeout_ns, g.status);
+    if (lane == 0 && !mbar_wait_bounded(B(C.acc), 0u, deadline, g.status))
+      mbar_wait_bounded(B(C.acc), 0u, globaltimer_ns() + g.timeout_ns, g.status);
     __syncwarp();
     tc_fence_after();
-    const int lg = warp & 3;                // TMEM lanes 32 lg .. 32 lg + 31 = tile rows
+    constexpr int CG = NPROD / 128;         // warps per TMEM lane group
+    const int lg = warp & 3, cg = warp >> 2;
     const int rw = row0 + lg * 32 + lane;   // the output row of this lane
     const uint32_t tl = tmem + ((uint32_t)(lg * 32) << 16);
-    for (int c0 = 16 * hf; c0 < TN; c0 += 32) {  // the two warps of a lane group alternate 16-column chunks
+    for (int c0 = 16 * cg; c0 < TN; c0 += 16 * CG) {
       float v0[16], v1[16];
       tmem_ld16(tl + (uint32_t)c0, v0);
       if (NMAT == 2) tmem_ld16(tl + (uint32_t)(TN + c0), v1);
@@ -585,32 +702,108 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
         }
       }
     }
-  } else if (lane == 0) {
+  } else if (KQ && warp >= W_LOAD && warp < W_LOAD + NLW) {
+    // ---------------------------------------------------- raw loaders
+    if constexpr (KQ) {
+      const int t = tid - W_LOAD * 32;
+      const uint8_t* Am[2] = {A0, A1};
+      const uint32_t raw_base = smem_u32(sm);
+      const int nunits = nk / (AK == A_Q2K ? 2 : 4);
+      for (int v = 0; v < nunits; ++v) {
+        const int buf = v % RAWN;
+        // wait until every producer has read the unit that used this buffer
+        if (v >= RAWN && !mbar_wait_bounded(B(C.raw_free[buf]), (uint32_t)((v / RAWN - 1) & 1), deadline, g.status))
+          break;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          const uint32_t dst0 = raw_base + PL::raw_off(m, buf);
+          for (int idx = t; idx < TM * RG::words(); idx += NLW * 32) {
+            const int rr = idx / RG::words(), w = idx - rr * RG::words();
+            if (row0 + rr >= g.a_rows) continue;
+            const uint8_t* rowp = Am[m] + (size_t)(row0 + rr) * g.a_row_bytes;
+            const uint32_t* src;
+            if constexpr (AK == A_Q2K) {
+              const int b = v >> 1, h = v & 1;
+              const int bw = w < 8 ? 4 + 8 * h + w : (w < 10 ? 2 * h + (w - 8) : 20);
+              src = reinterpret_cast<const uint32_t*>(rowp + (size_t)b * Q2K_B) + bw;
+            } else {
+              const uintptr_t a = reinterpret_cast<uintptr_t>(rowp + (size_t)v * Q3K_B);
+              src = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3)) + w;
+            }
+            cp_async4(dst0 + (uint32_t)(rr * RG::PITCH + w) * 4u, src);
+          }
+        }
+        cp_async_arrive(B(C.raw_full[buf]));  // once this thread's copies have landed
+      }
+      // copies still in flight land before the block can exit
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+  } else if (warp == W_TMA && lane == 0) {
+    // ------------------------------------------------------- TMA issuer
+    const bool boxed = g.tiles != nullptr;  // expert jobs: B_BOX-row boxes up to TN rows
+    const uint32_t bbytes = (uint32_t)(BMODE == B_GATHER || boxed ? TN : TNM) * 128u;
+    const uint32_t bytes = (KQ ? 0u : NMAT * A_TILE) + PL::NPART * bbytes;
+    for (int kc = 0; kc < nk; ++kc) {
+      const int sb = kc % NSB;
+      if (kc >= NSB && !mbar_wait_bounded(B(C.empty_b[sb]), (uint32_t)((kc / NSB - 1) & 1), deadline, g.status)) break;
+      uint64_t* fb = B(C.full_b[sb]);
+      mbar_arrive_expect_tx(fb, bytes);
+      if constexpr (!KQ) {
+#pragma unroll
+        for (int mat = 0; mat < NMAT; ++mat)
+          tma_load_2d(smem_u32(sm + PL::a_off(sb, mat, 0)), &g.map_a[mat], kc * KC, row0, fb);
+      }
+#pragma unroll
+      for (int pt = 0; pt < PL::NPART; ++pt) {
+        const uint32_t dst = smem_u32(sm + PL::b_off(sb, pt));
+        if constexpr (BMODE == B_GATHER) {
+          for (int i = 0; i < TN; i += 4)
+            tma_gather4(dst + (uint32_t)i * 128u, &g.map_b[pt], kc * KC, s_rows[i], s_rows[i + 1], s_rows[i + 2],
+                        s_rows[i + 3], fb);
+        } else if (boxed) {
+          for (int i = 0; i < TN; i += B_BOX) tma_load_2d(dst + (uint32_t)i * 128u, &g.map_b[pt], kc * KC, col0 + i, fb);
+        } else {
+          tma_load_2d(dst, &g.map_b[pt], kc * KC, col0, fb);
+        }
+      }
+    }
+  } else if (warp == W_MMA && lane == 0) {
     // ----------------------------------------------------- MMA issuer
     const uint32_t idesc = umma_idesc(TN, AK == A_BF16);
     for (int kc = 0; kc < nk; ++kc) {
-      const int s = kc % NS;
-      if (!mbar_wait_bounded(reinterpret_cast<uint64_t*>(&C.full[s]), (uint32_t)((kc / NS) & 1), deadline, g.status))
-        break;
+      const int sb = kc % NSB, sa = KQ ? kc % NSA : sb;
+      if (!mbar_wait_bounded(B(C.full_b[sb]), (uint32_t)((kc / NSB) & 1), deadline, g.status)) break;
+      if (KQ && !mbar_wait_bounded(B(C.full_a[sa]), (uint32_t)((kc / NSA) & 1), deadline, g.status)) break;
       tc_fence_after();
-      const uint32_t st = smem_u32(sm + (size_t)s * PL::STAGE);
+      const uint32_t base = smem_u32(sm);
 #pragma unroll
       for (int mat = 0; mat < NMAT; ++mat) {
         const uint32_t td = tmem + (uint32_t)(mat * TN);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint64_t ah = umma_desc(st + PL::a_off(mat, 0) + 32u * k);
-          const uint64_t bh = umma_desc(st + PL::b_off(0) + 32u * k);
-          umma_f16(td, ah, bh, idesc, (kc | k) ? 1u : 0u);
-          if (SPLIT) {
-            umma_f16(td, ah, umma_desc(st + PL::b_off(SPLIT ? 1 : 0) + 32u * k), idesc, 1u);
-            umma_f16(td, umma_desc(st + PL::a_off(mat, SPLIT ? 1 : 0) + 32u * k), bh, idesc, 1u);
+          const uint64_t bh = umma_desc(base + PL::b_off(sb, 0) + 32u * k);
+          if constexpr (PL::ATMEM) {
+            // A in tensor memory: 8 columns (16 K values) per MMA
+            const uint32_t ta = tmem + 256u + (uint32_t)(sa * PL::TA_COLS + (mat * PL::NPART) * 32 + 8 * k);
+            umma_f16_ta(td, ta, bh, idesc, (kc | k) ? 1u : 0u);
+            if (SPLIT) {
+              umma_f16_ta(td, ta, umma_desc(base + PL::b_off(sb, SPLIT ? 1 : 0) + 32u * k), idesc, 1u);
+              umma_f16_ta(td, ta + 32u, bh, idesc, 1u);
+            }
+          } else {
+            const uint64_t ah = umma_desc(base + PL::a_off(sa, mat, 0) + 32u * k);
+            umma_f16(td, ah, bh, idesc, (kc | k) ? 1u : 0u);
+            if (SPLIT) {
+              umma_f16(td, ah, umma_desc(base + PL::b_off(sb, SPLIT ? 1 : 0) + 32u * k), idesc, 1u);
+              umma_f16(td, umma_desc(base + PL::a_off(sa, mat, SPLIT ? 1 : 0) + 32u * k), bh, idesc, 1u);
+            }
           }
         }
       }
-      umma_commit(reinterpret_cast<uint64_t*>(&C.empty[s]));
+      umma_commit(B(C.empty_b[sb]));
+      if (KQ) umma_commit(B(C.empty_a[sa]));
     }
-    umma_commit(reinterpret_cast<uint64_t*>(&C.acc));
+    umma_commit(B(C.acc));
   }
   __syncwarp();
   tc_fence_before();
@@ -621,31 +814,63 @@ __global__ void __launch_bounds__(GTHREADS, 1) k_gemm(const __grid_constant__ Ge
   }
 }
 
-template <int AK, int NMAT, bool SPLIT, int EPI, int TNM, int NS>
+template <int AK, int NMAT, bool SPLIT, int EPI, int TNM, int NSA, int NSB, int RAWN, int NPROD, int BMODE>
 int launch_gemm(const GemmArgs& g, unsigned grid, cudaStream_t s) {
-  constexpr size_t smem = Plan<NMAT, SPLIT, TNM, NS>::SMEM;
+  constexpr size_t smem = Plan<AK, NMAT, SPLIT, TNM, NSA, NSB, RAWN>::SMEM;
   static_assert(smem <= 232448, "GEMM stages exceed the shared memory of a block");
+  auto kern = k_gemm<AK, NMAT, SPLIT, EPI, TNM, NSA, NSB, RAWN, NPROD, BMODE>;
   static int attr_dev = -1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (attr_dev != dev) {
-    if (cudaFuncSetAttribute(k_gemm<AK, NMAT, SPLIT, EPI, TNM, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr_dev = dev;
   }
   if (grid == 0) return MOE_OK;
-  k_gemm<AK, NMAT, SPLIT, EPI, TNM, NS><<<grid, GTHREADS, smem, s>>>(g);
+  kern<<<grid, NPROD + 32 * loader_warps<AK>() + 64, smem, s>>>(g);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// A row-major matrix of 16-bit values [rows][cols] (cols a multiple of 64,
+// row pitch a multiple of 16 bytes) read in boxes of 64 values x box_rows
+// rows into 128-byte-swizzled shared memory; rows past the end read zeros.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base || rows == 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int NP_KQ = 512;   // K-quant GEMMs: 16 dequantising warps
+constexpr int NP_BF = 128;   // bf16 GEMMs: 4 epilogue warps
+
 int route_steps(const PrefillParams& p, cudaStream_t s) {
   GemmArgs g{};
-  g.K = p.D; g.a_rows = p.N; g.a_row_bytes = 2 * p.D; g.a0 = reinterpret_cast<const uint8_t*>(p.router_w);
-  g.pseudo = -1; g.b = p.x; g.cols = p.m; g.mt_count = (p.N + TM - 1) / TM;
+  if (!make_map(&g.map_a[0], p.router_w, p.D, p.N, TM) || !make_map(&g.map_b[0], p.x, p.D, p.m, PF_TN))
+    return MOE_ERR_CUDA;
+  g.K = p.D; g.a_rows = p.N; g.pseudo = -1; g.cols = p.m; g.mt_count = (p.N + TM - 1) / TM;
   g.out_f32 = p.logits; g.out_ld = p.N; g.status = &p.ctrl->status; g.timeout_ns = p.timeout_ns;
   const unsigned grid = (unsigned)(g.mt_count * ((p.m + PF_TN - 1) / PF_TN));
-  int rc = launch_gemm<A_BF16, 1, false, E_F32, PF_TN, 4>(g, grid, s);
+  int rc = launch_gemm<A_BF16, 1, false, E_F32, PF_TN, 4, 4, 1, NP_BF, B_TILED>(g, grid, s);
   if (rc) return rc;
   SelectParams sp{};
   sp.logits = p.logits; sp.bias = p.bias; sp.m = p.m; sp.N = p.N; sp.k = p.k; sp.norm = p.norm;
@@ -665,9 +890,10 @@ int launch_prefill(const PrefillParams& p, cudaStream_t s) {
   const int shq = p.shared_kind == MOE_SHARED_KQUANT;
   const int NE = N + 1;
   const int nch = (m + PF_GCH - 1) / PF_GCH;
+  const int V = m * k + (shq ? m : 0);  // pair rows (the K-quant shared expert's tokens included)
   int rc;
-  uint16_t* x16h = reinterpret_cast<uint16_t*>(pw + L.x16h);
-  uint16_t* x16l = reinterpret_cast<uint16_t*>(pw + L.x16l);
+  uint16_t* xgh = reinterpret_cast<uint16_t*>(pw + L.xgh);
+  uint16_t* xgl = reinterpret_cast<uint16_t*>(pw + L.xgl);
   int* chunk = reinterpret_cast<int*>(pw + L.chunk);
   int* offsets = reinterpret_cast<int*>(pw + L.offsets);
   int* expert_ok = reinterpret_cast<int*>(pw + L.expert_ok);
@@ -683,54 +909,64 @@ int launch_prefill(const PrefillParams& p, cudaStream_t s) {
   uint16_t* hs = reinterpret_cast<uint16_t*>(pw + L.hs);
   float* sp = reinterpret_cast<float*>(pw + L.sp);
 
-  // 1. fp16 of q8_1(x)
-  {
-    const long nb = (long)m * (D / 32);
-    long blocks = (nb + 255) / 256;
-    if (blocks > 152L * 8) blocks = 152L * 8;
-    k_x16<<<(unsigned)blocks, 256, 0, s>>>(p.x, m, D, x16h, x16l);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  }
-  // 2-3. router logits and selection
+  // 1-2. router logits and selection
   if ((rc = route_steps(p, s))) return rc;
-  // 4. grouping
+  // 3. grouping
   k_group_hist<<<nch, 256, NE * sizeof(int), s>>>(p.topk_idx, m, k, N, shq, chunk);
   k_group_scan<<<1, 1024, 0, s>>>(chunk, nch, N, p.expert_ptrs, I / TM, D / TM, offsets, expert_ok, gu_tiles, dn_tiles,
                                   n_tiles, &p.ctrl->status);
   k_group_scatter<<<nch, 256, 0, s>>>(p.topk_idx, p.topk_w, m, k, N, shq, chunk, pair_tok, pair_w, pos_of, pos_sh);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  // 4. the q8_1 values of x as fp16 high and low parts, in pair order
+  {
+    const long nb = (long)m * (D / 32);
+    long blocks = (nb + 255) / 256;
+    if (blocks > 152L * 8) blocks = 152L * 8;
+    k_xg<<<(unsigned)blocks, 256, 0, s>>>(p.x, m, D, k, pos_of, shq ? pos_sh : nullptr, xgh, xgl);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
   // 5. gate/up of the routed experts (and of a K-quant shared expert) -> fp16 of q8_1(h)
   {
     GemmArgs g{};
+    if (!make_map(&g.map_b[0], xgh, D, V, B_BOX) || !make_map(&g.map_b[1], xgl, D, V, B_BOX))
+      return MOE_ERR_CUDA;
     g.K = D; g.a_rows = I; g.a_row_bytes = (D / QK) * Q2K_B; g.eptr = p.expert_ptrs; g.pj0 = 0; g.pj1 = 1;
-    g.pseudo = shq ? N : -1; g.a0 = p.sh1; g.a1 = p.sh3; g.b = x16h; g.b_lo = x16l; g.b_rows = pair_tok;
+    g.pseudo = shq ? N : -1; g.a0 = p.sh1; g.a1 = p.sh3;
     g.tiles = gu_tiles; g.n_tiles = n_tiles; g.offsets = offsets; g.out_h = h16; g.out_ld = I;
     g.swiglu_limit = p.swiglu_limit; g.status = &p.ctrl->status; g.timeout_ns = p.timeout_ns;
     const unsigned grid = (unsigned)L.max_gu_tiles * (unsigned)(I / TM);
-    if ((rc = launch_gemm<A_Q2K, 2, true, E_SWIGLU_Q8, PF_TN_GU, 2>(g, grid, s))) return rc;
+    if ((rc = launch_gemm<A_Q2K, 2, true, E_SWIGLU_Q8, PF_TN_GU, 2, 4, 4, NP_KQ, B_TILED>(g, grid, s))) return rc;
   }
   // 6. down -> E per pair
   {
     GemmArgs g{};
+    if (!make_map(&g.map_b[0], h16, I, V, B_BOX)) return MOE_ERR_CUDA;
     g.K = I; g.a_rows = D; g.a_row_bytes = (I / QK) * Q3K_B; g.eptr = p.expert_ptrs; g.pj0 = 2; g.pj1 = 2;
-    g.pseudo = shq ? N : -1; g.a0 = p.sh2; g.b = h16;
+    g.pseudo = shq ? N : -1; g.a0 = p.sh2;
     g.tiles = dn_tiles; g.n_tiles = n_tiles + 1; g.offsets = offsets; g.out_f32 = ep; g.out_ld = D;
     g.status = &p.ctrl->status; g.timeout_ns = p.timeout_ns;
     const unsigned grid = (unsigned)L.max_dn_tiles * (unsigned)(D / TM);
-    if ((rc = launch_gemm<A_Q3K, 1, false, E_F32, PF_TN, 4>(g, grid, s))) return rc;
+    if ((rc = launch_gemm<A_Q3K, 1, false, E_F32, PF_TN, 4, 4, 4, NP_KQ, B_TILED>(g, grid, s))) return rc;
   }
   // 7. the bf16 shared expert
   if (!shq) {
     const unsigned ntok = (unsigned)((m + PF_TN - 1) / PF_TN);
     GemmArgs g{};
-    g.K = D; g.a_rows = I; g.a_row_bytes = 2 * D; g.a0 = p.sh1; g.a1 = p.sh3; g.pseudo = -1; g.b = p.x; g.cols = m;
+    if (!make_map(&g.map_a[0], p.sh1, D, I, TM) || !make_map(&g.map_a[1], p.sh3, D, I, TM) ||
+        !make_map(&g.map_b[0], p.x, D, m, PF_TN))
+      return MOE_ERR_CUDA;
+    g.K = D; g.a_rows = I; g.pseudo = -1; g.cols = m;
     g.mt_count = I / TM; g.out_h = hs; g.out_ld = I; g.swiglu_limit = p.swiglu_limit;
     g.status = &p.ctrl->status; g.timeout_ns = p.timeout_ns;
-    if ((rc = launch_gemm<A_BF16, 2, false, E_SWIGLU_BF16, PF_TN, 3>(g, (unsigned)g.mt_count * ntok, s))) return rc;
+    if ((rc = launch_gemm<A_BF16, 2, false, E_SWIGLU_BF16, PF_TN, 3, 3, 1, NP_BF, B_TILED>(g, (unsigned)g.mt_count * ntok,
+                                                                                      s)))
+      return rc;
     GemmArgs d{};
-    d.K = I; d.a_rows = D; d.a_row_bytes = 2 * I; d.a0 = p.sh2; d.pseudo = -1; d.b = hs; d.cols = m;
+    if (!make_map(&d.map_a[0], p.sh2, I, D, TM) || !make_map(&d.map_b[0], hs, I, m, PF_TN)) return MOE_ERR_CUDA;
+    d.K = I; d.a_rows = D; d.pseudo = -1; d.cols = m;
     d.mt_count = D / TM; d.out_f32 = sp; d.out_ld = D; d.status = &p.ctrl->status; d.timeout_ns = p.timeout_ns;
-    if ((rc = launch_gemm<A_BF16, 1, false, E_F32, PF_TN, 4>(d, (unsigned)d.mt_count * ntok, s))) return rc;
+    if ((rc = launch_gemm<A_BF16, 1, false, E_F32, PF_TN, 4, 4, 1, NP_BF, B_TILED>(d, (unsigned)d.mt_count * ntok, s)))
+      return rc;
   }
   // 8. ordered combine
   k_combine<<<m, 256, 0, s>>>(p.topk_idx, pos_of, expert_ok, pair_w, ep, sp, shq ? pos_sh : nullptr, k, D, p.out);
