@@ -184,7 +184,6 @@ int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const void* ro
   dp.xu = reinterpret_cast<int*>(w + L.xu);
   dp.hu = reinterpret_cast<int*>(w + L.hu);
   dp.shh = w + L.shh;
-  dp.plan_w = reinterpret_cast<DecodePlan*>(w + L.plan);
   const int Td = cfg->max_tokens < DECODE_MAX_M ? cfg->max_tokens : DECODE_MAX_M;
   dp.shvec0 = Td * cfg->topk;
   dp.out = out;

@@ -30,15 +30,15 @@ struct Ctrl {
   unsigned ticket;        // work tickets of the fused decode kernel
   unsigned q8_done;       // q8_1(x) tasks finished
   unsigned router_done;   // router tasks finished
-  unsigned route_ready;   // the decode plan is written
+  unsigned reserved;
   unsigned shgu_done;     // shared-expert gate/up tasks finished
   unsigned rtgu_done;     // routed gate/up tasks finished
   unsigned exit_count;    // blocks that have left the fused kernel
   unsigned pad[55];
 };
 
-// Routing of a decode call grouped by expert (ascending id), written by the
-// warp that finishes the last router task.
+// Routing of a decode call grouped by expert (ascending id), built in shared
+// memory by each block's planner warp.
 struct alignas(16) DecodePlan {
   int n_exp;                         // distinct experts picked
   int n_pairs;                       // m * topk

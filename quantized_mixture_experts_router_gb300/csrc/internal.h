@@ -48,14 +48,14 @@ struct DecodeParams {
   int* xu;                   // unit layout of q8_1(x) (when not kept in shared memory)
   int* hu;                   // unit layout of q8_1(h), one per vector (pairs, then shared tokens)
   uint8_t* shh;              // bf16 shared expert: h [m, I] bf16
-  DecodePlan* plan_w;
   int shvec0;                // first vector index of the shared expert's tokens
   float* out;                // f32 [m, D]
   Ctrl* ctrl;
   unsigned long long timeout_ns;
   // shared-memory plan of the launch (set by launch_decode_layer); a cache
   // offset of 0 means "not cached, read from global memory"
-  uint32_t sm_ctl, sm_plan, sm_items, item_bytes, sm_sel, sm_xb, sm_ep, ep_bytes, sm_x, sm_hr, sm_hs, smem_bytes;
+  uint32_t sm_ctl, sm_plan, sm_items, item_bytes, sm_sel, sm_xb, sm_ep, ep_bytes, sm_x, sm_hr, sm_hs, sm_bias,
+      smem_bytes;
 };
 
 struct PrefillParams {

@@ -34,7 +34,9 @@ namespace moe {
 namespace {
 
 constexpr int NCW = 8;               // consumer warps
-constexpr int NTH = (NCW + 1) * 32;  // + producer warp
+constexpr int W_PROD = NCW;          // the producer warp
+constexpr int W_PLAN = NCW + 1;      // the planner warp: this block's copy of the routing
+constexpr int NTH = (NCW + 2) * 32;
 constexpr int SB = 20480;            // bytes per ring stage
 constexpr int NST = 8;               // ring stages
 constexpr int NIS = 4;               // item state slots
@@ -48,8 +50,8 @@ constexpr int SDR = 4;               // shared bf16 down rows per stage
 
 enum : int { K_STOP = 0, K_Q8, K_ROUTER, K_SHGU_B, K_GU_Q, K_DN_SHB, K_DN_SHQ, K_DN_RT };
 enum : int { I_Q8 = 0, I_ROUTER, I_SHGU_B, I_GU, I_DN };
-// shared-memory copies: x (bf16), routed h units, shared h, q8_1(x) units, expert pointer table
-enum : int { CB_XB = 0, CB_HR, CB_HS, CB_XU, CB_EP };
+// shared-memory copies: x (bf16), routed h units, shared h, q8_1(x) units, expert pointer table, bias
+enum : int { CB_XB = 0, CB_HR, CB_HS, CB_XU, CB_EP, CB_BIAS, N_CB };
 
 struct Hdr {
   int kind, slot, a, b;
@@ -66,9 +68,9 @@ struct Ctl {
   unsigned long long full[NST];
   unsigned long long empty[NST];
   unsigned long long item_done[NIS];
-  unsigned long long pbar;     // the block's copy of the plan has landed
-  unsigned long long cbar[5];  // shared-memory copies: see CB_*
-  unsigned cstate[5];          // 0 empty, 1 being filled
+  unsigned long long pbar;        // the block's plan is built
+  unsigned long long cbar[N_CB];  // shared-memory copies: see CB_*
+  unsigned cstate[N_CB];          // 0 empty, 1 being filled
   unsigned next;               // consumer grab counter
 };
 
@@ -145,11 +147,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ void dot8(float& acc, const uint4& w, const uint4& x) {
-  acc = fmaf(bf16lo(w.x), bf16lo(x.x), acc); acc = fmaf(bf16hi(w.x), bf16hi(x.x), acc);
-  acc = fmaf(bf16lo(w.y), bf16lo(x.y), acc); acc = fmaf(bf16hi(w.y), bf16hi(x.y), acc);
-  acc = fmaf(bf16lo(w.z), bf16lo(x.z), acc); acc = fmaf(bf16hi(w.z), bf16hi(x.z), acc);
-  acc = fmaf(bf16lo(w.w), bf16lo(x.w), acc); acc = fmaf(bf16hi(w.w), bf16hi(x.w), acc);
+// 8 bf16 products into two accumulators (two independent FMA chains)
+__device__ __forceinline__ void dot8(float2& acc, const uint4& w, const uint4& x) {
+  acc.x = fmaf(bf16lo(w.x), bf16lo(x.x), acc.x); acc.y = fmaf(bf16hi(w.x), bf16hi(x.x), acc.y);
+  acc.x = fmaf(bf16lo(w.y), bf16lo(x.y), acc.x); acc.y = fmaf(bf16hi(w.y), bf16hi(x.y), acc.y);
+  acc.x = fmaf(bf16lo(w.z), bf16lo(x.z), acc.x); acc.y = fmaf(bf16hi(w.z), bf16hi(x.z), acc.y);
+  acc.x = fmaf(bf16lo(w.w), bf16lo(x.w), acc.x); acc.y = fmaf(bf16hi(w.w), bf16hi(x.w), acc.y);
 }
 
 // an activation unit: from shared memory, or (written by other blocks in
@@ -237,9 +240,11 @@ __device__ void ensure_cache(Ctx& c, int which, const unsigned* counter, unsigne
 
 // ------------------------------------------------------------- the plan
 // Selection for every token and grouping of the (expert, token) pairs by
-// ascending expert id; run by the one warp that finished the router.  It
-// keeps its intermediate values in shared memory: under full load every
-// dependent global round trip costs about a microsecond.
+// ascending expert id, into this block's shared-memory plan; run by the
+// planner warp of every block once all router rows are done (every block
+// computes the same plan; block 0 also writes the routing outputs).  Under
+// full load every dependent global round trip costs microseconds, so the
+// plan never goes through global memory.
 __device__ void build_plan(Ctx& c) {
   const DecodeParams& p = c.p;
   const int lane = threadIdx.x & 31;
@@ -248,15 +253,16 @@ __device__ void build_plan(Ctx& c) {
   float* pk_w = reinterpret_cast<float*>(pk_id + MAXP);
   int* s_e = pk_id + 2 * MAXP;  // expert of each sorted position
   int* s_t = pk_id + 3 * MAXP;  // token of each sorted position
+  const bool writer = blockIdx.x == 0;
   for (int t = 0; t < p.m; ++t) {
+    float* wo = writer ? p.topk_w + (size_t)t * p.k : pk_w + t * p.k;
+    int* io = writer ? p.topk_idx + (size_t)t * p.k : pk_id + t * p.k;
     if (p.N <= 384)
       route_token_warp_r12(p.logits + (size_t)t * p.N, p.sk + (size_t)t * p.N, p.bias, p.N, p.k, p.gate_temp,
-                           p.norm, p.route_scale, p.topk_w + (size_t)t * p.k, p.topk_idx + (size_t)t * p.k,
-                           &p.ctrl->status, scratch, pk_id + t * p.k, pk_w + t * p.k);
+                           p.norm, p.route_scale, wo, io, &p.ctrl->status, scratch, pk_id + t * p.k, pk_w + t * p.k);
     else
       route_token_warp(p.logits + (size_t)t * p.N, p.sk + (size_t)t * p.N, p.bias, p.N, p.k, p.gate_temp, p.norm,
-                       p.route_scale, p.topk_w + (size_t)t * p.k, p.topk_idx + (size_t)t * p.k, &p.ctrl->status,
-                       scratch, pk_id + t * p.k, pk_w + t * p.k);
+                       p.route_scale, wo, io, &p.ctrl->status, scratch, pk_id + t * p.k, pk_w + t * p.k);
   }
   // the expert pointer table: the block's copy when there is one
   const unsigned long long* eptr = p.expert_ptrs;
@@ -266,7 +272,7 @@ __device__ void build_plan(Ctx& c) {
   }
   const unsigned long long* eptr_s = reinterpret_cast<const unsigned long long*>(smem_base() + p.sm_ep);
   __syncwarp();
-  DecodePlan* plan = p.plan_w;
+  DecodePlan* plan = reinterpret_cast<DecodePlan*>(smem_base() + p.sm_plan);
   const int P = p.m * p.k;
   for (int i = lane; i < P; i += 32) {
     const int e = pk_id[i], t = i / p.k;
@@ -298,7 +304,7 @@ __device__ void build_plan(Ctx& c) {
         ptr[j] = (w + 1) * 8 <= p.ep_bytes ? eptr_s[w] : eptr[w];
       }
       for (int j = 0; j < 3; ++j) bad |= (ptr[j] == 0ull) || (ptr[j] & 255ull);
-      if (bad) atomicOr(&p.ctrl->status, (unsigned)MOE_STATUS_MISSING_EXPERT);
+      if (bad && writer) atomicOr(&p.ctrl->status, (unsigned)MOE_STATUS_MISSING_EXPERT);
       for (int j = 0; j < 3; ++j) plan->exp_ptr[slot][j] = bad ? 0ull : ptr[j];
     }
     n_exp += __popc(bal);
@@ -349,22 +355,25 @@ __device__ void task_router(Ctx& c, const uint8_t* stage, int r0) {
   const uint4* w = reinterpret_cast<const uint4*>(stage);
   const int rows = min(RR, p.N - r0);
   need_xb(c);
+  if (p.sm_bias && (threadIdx.x & 31) == 0) mbar_wait_bounded(bar(c.C.cbar[CB_BIAS]), 0u, c.deadline, &p.ctrl->status);
+  __syncwarp();
+  const float* bias = p.sm_bias ? reinterpret_cast<const float*>(smem_base() + p.sm_bias) : p.bias;
   for (int t = 0; t < p.m; ++t) {
-    float a0 = 0.f, a1 = 0.f;
-    for (int ch = lane; ch < chunks; ch += 32) {
+    float2 a0[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, a1[2] = {a0[0], a0[0]};
+    for (int ch = lane, i = 0; ch < chunks; ch += 32, ++i) {
       const uint4 xv = x_chunk(p, t, ch);
-      dot8(a0, w[ch], xv);
-      if (rows > 1) dot8(a1, w[chunks + ch], xv);
+      dot8(a0[i & 1], w[ch], xv);
+      if (rows > 1) dot8(a1[i & 1], w[chunks + ch], xv);
     }
-    a0 = warp_sum(a0);
-    a1 = warp_sum(a1);
+    const float s0 = warp_sum((a0[0].x + a0[0].y) + (a0[1].x + a0[1].y));
+    const float s1 = warp_sum((a1[0].x + a1[0].y) + (a1[1].x + a1[1].y));
     // the logit, and the fast score and key the selection starts from
     if (lane < rows) {
-      const float z = lane == 0 ? a0 : a1;
+      const float z = lane == 0 ? s0 : s1;
       const int e = r0 + lane;
       const float sc = score_fast(z, p.gate_temp);
       p.logits[(size_t)t * p.N + e] = z;
-      p.sk[(size_t)t * p.N + e] = make_float2(sc, __fadd_rn(sc, __ldg(p.bias + e)));
+      p.sk[(size_t)t * p.N + e] = make_float2(sc, __fadd_rn(sc, bias[e]));
     }
   }
 }
@@ -377,14 +386,14 @@ __device__ void task_shgu_b(Ctx& c, const uint8_t* stage, int row) {
   const uint4* w = reinterpret_cast<const uint4*>(stage);
   need_xb(c);
   for (int t = 0; t < p.m; ++t) {
-    float g = 0.f, u = 0.f;
-    for (int ch = lane; ch < chunks; ch += 32) {
+    float2 ga[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, ua[2] = {ga[0], ga[0]};
+    for (int ch = lane, i = 0; ch < chunks; ch += 32, ++i) {
       const uint4 xv = x_chunk(p, t, ch);
-      dot8(g, w[ch], xv);
-      dot8(u, w[chunks + ch], xv);
+      dot8(ga[i & 1], w[ch], xv);
+      dot8(ua[i & 1], w[chunks + ch], xv);
     }
-    g = warp_sum(g);
-    u = warp_sum(u);
+    const float g = warp_sum((ga[0].x + ga[0].y) + (ga[1].x + ga[1].y));
+    const float u = warp_sum((ua[0].x + ua[0].y) + (ua[1].x + ua[1].y));
     if (lane == 0)
       reinterpret_cast<__nv_bfloat16*>(p.shh)[(size_t)t * p.I + row] =
           __float2bfloat16_rn(swiglu_f32(g, u, p.swiglu_limit));
@@ -518,9 +527,9 @@ __device__ void task_dn_b(Ctx& c, const uint8_t* stage, int part, float* ib) {
   const uint4* w = reinterpret_cast<const uint4*>(stage);
   for (int t = 0; t < p.m; ++t) {
     const uint4* hr = hbase + (size_t)t * chunks;
-    float acc[SDR];
+    float2 acc[SDR];
 #pragma unroll
-    for (int r = 0; r < SDR; ++r) acc[r] = 0.f;
+    for (int r = 0; r < SDR; ++r) acc[r] = make_float2(0.f, 0.f);
     for (int ch = lane; ch < chunks; ch += 32) {
       const uint4 hv = hs ? hr[ch] : __ldcg(hr + ch);
 #pragma unroll
@@ -528,7 +537,7 @@ __device__ void task_dn_b(Ctx& c, const uint8_t* stage, int part, float* ib) {
     }
 #pragma unroll
     for (int r = 0; r < SDR; ++r) {
-      const float s = warp_sum(acc[r]);
+      const float s = warp_sum(acc[r].x + acc[r].y);
       if (lane == 0) ib[(P + t) * DG + part * SDR + r] = s;
     }
   }
@@ -543,20 +552,10 @@ __device__ void complete_item(Ctx& c, const Item& it, float* ib) {
       __threadfence();
       if (lane == 0) atomicAdd(&p.ctrl->q8_done, 1u);
       break;
-    case I_ROUTER: {
+    case I_ROUTER:
       __threadfence();
-      unsigned old = 0;
-      if (lane == 0) old = atomicAdd(&p.ctrl->router_done, 1u);
-      old = __shfl_sync(0xffffffffu, old, 0);
-      if (old == (unsigned)c.z.n_router - 1u) {
-        __threadfence();
-        build_plan(c);
-        __threadfence();
-        if (lane == 0)
-          asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&p.ctrl->route_ready), "r"(1u) : "memory");
-      }
+      if (lane == 0) atomicAdd(&p.ctrl->router_done, 1u);
       break;
-    }
     case I_SHGU_B:
       __threadfence();
       if (lane == 0) atomicAdd(&p.ctrl->shgu_done, 1u);
@@ -611,7 +610,7 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     }
     for (int i = 0; i < NIS; ++i) mbar_init(bar(C.item_done[i]), 1);
     mbar_init(bar(C.pbar), 1);
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < N_CB; ++i) {
       mbar_init(bar(C.cbar[i]), 1);
       C.cstate[i] = 0u;
     }
@@ -622,7 +621,26 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
   const Sizes z = sizes_of(p);
   const int groups = p.D / DG;
 
-  if (warp == NCW) {
+  if (warp == W_PLAN) {
+    // ----------------------------------------------------------- planner
+    // Wait for every router row of the call, then build this block's plan.
+    // On a timeout the plan is left empty (no routed expert work) so the
+    // block still finishes; the status word already says why.
+    Ctx c{p, z, C, deadline, -1, false, false, false, false, false};
+    bool ok = true;
+    if (lane == 0) ok = wait_count(&p.ctrl->router_done, (unsigned)z.n_router, deadline, &p.ctrl->status);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+      build_plan(c);
+    } else if (lane == 0) {
+      DecodePlan* plan = reinterpret_cast<DecodePlan*>(smem_base() + p.sm_plan);
+      plan->n_exp = 0;
+      plan->n_pairs = 0;
+      plan->exp_off[0] = 0;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(C.pbar));
+  } else if (warp == W_PROD) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       // x and the expert pointer table are inputs of the call: copy them to
@@ -636,6 +654,10 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
         mbar_arrive_expect_tx(bar(C.cbar[CB_EP]), p.ep_bytes);
         bulk_g2s(smem_base() + p.sm_ep, p.expert_ptrs, p.ep_bytes, bar(C.cbar[CB_EP]));
       }
+      if (p.sm_bias) {
+        mbar_arrive_expect_tx(bar(C.cbar[CB_BIAS]), (uint32_t)(p.N * 4));
+        bulk_g2s(smem_base() + p.sm_bias, p.bias, (uint32_t)(p.N * 4), bar(C.cbar[CB_BIAS]));
+      }
       uint32_t n = 0;  // stages issued
       uint32_t j = 0;  // items started
       int n_exp = -1;
@@ -646,11 +668,7 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
         const unsigned t = t_next;
         Item it = decode_ticket(t, z, groups, n_exp);
         if (it.kind == -1) {
-          if (!(ok = wait_count(&p.ctrl->route_ready, 1u, deadline, &p.ctrl->status))) break;
-          // the block's own copy of the plan, read by everyone from here on
-          asm volatile("fence.proxy.async;" ::: "memory");
-          mbar_arrive_expect_tx(bar(C.pbar), (uint32_t)sizeof(DecodePlan));
-          bulk_g2s(smem_base() + p.sm_plan, p.plan_w, (uint32_t)sizeof(DecodePlan), bar(C.pbar));
+          // the block's plan, built by the planner warp
           if (!(ok = mbar_wait_bounded(bar(C.pbar), 0u, deadline, &p.ctrl->status))) break;
           n_exp = reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan)->n_exp;
           it = decode_ticket(t, z, groups, n_exp);
@@ -824,7 +842,6 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
       p.ctrl->ticket = 0u;
       p.ctrl->q8_done = 0u;
       p.ctrl->router_done = 0u;
-      p.ctrl->route_ready = 0u;
       p.ctrl->shgu_done = 0u;
       p.ctrl->rtgu_done = 0u;
       __threadfence();
@@ -865,6 +882,8 @@ bool plan_smem(DecodeParams& p) {
   p.sm_x = try_cache((size_t)p.m * unit_bytes(p.D));
   p.sm_hr = try_cache(P * unit_bytes(p.I));
   p.sm_hs = try_cache(p.shared_kind == MOE_SHARED_BF16 ? (size_t)p.m * 2 * p.I : (size_t)p.m * unit_bytes(p.I));
+  // the bias, when a bulk copy can move it (16-B aligned, a multiple of 16 bytes)
+  p.sm_bias = (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0 && (p.N * 4) % 16 == 0 ? try_cache((size_t)p.N * 4) : 0u;
   p.smem_bytes = (uint32_t)off;
   return true;
 }

@@ -90,7 +90,6 @@ extern "C" int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, in
   dp.xu = reinterpret_cast<int*>(w + L.xu);
   dp.hu = reinterpret_cast<int*>(w + L.hu);
   dp.shh = w + L.shh;
-  dp.plan_w = reinterpret_cast<DecodePlan*>(w + L.plan);
   dp.shvec0 = c.max_tokens * c.topk;
   dp.out = out;
   dp.ctrl = reinterpret_cast<Ctrl*>(w + L.ctrl);
