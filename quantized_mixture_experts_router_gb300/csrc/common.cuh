@@ -296,42 +296,50 @@ __device__ __forceinline__ float q2k_unit_dot(const uint8_t* blk, int c, const X
   return d * acc_d - dmin * acc_m;
 }
 
-// 32-bit word at a 2-B aligned shared-memory address.
-__device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t* p) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* base = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-  const uint32_t sh = (uint32_t)(a & 3u) * 8u;
-  return __funnelshift_r(base[0], base[1], sh);
-}
-
 // Unit c of a Q3_K block (110 B, 2-B aligned, in shared memory) dotted with
 // the matching activation unit.  q = lo + 4 hb - 4 with lo the 2-bit plane j
 // and hb bit 4h + j of the hmask byte:
 //   sum_j dq_j * d * (code_j - 32) * ( sum(lo*qx) + 4 sum(hb*qx) - 4 sum(qx) )
+// The block's words are read from the 4-byte aligned window around it and
+// realigned with one byte permute each (the window may reach 2 bytes past the
+// block, still inside the stage buffer).
 __device__ __forceinline__ float q3k_unit_dot(const uint8_t* blk, int c, const XUnit& x) {
   const int h = c >> 1, half = c & 1;
-  const uint8_t* qs = blk + 32 + 16 * c;
-  const uint8_t* hm = blk + 16 * half;
-  const uint32_t q0 = lds_u32_a2(qs), q1 = lds_u32_a2(qs + 4), q2 = lds_u32_a2(qs + 8), q3 = lds_u32_a2(qs + 12);
-  const uint32_t m0 = lds_u32_a2(hm), m1 = lds_u32_a2(hm + 4), m2 = lds_u32_a2(hm + 8), m3 = lds_u32_a2(hm + 12);
-  const uint32_t s_lo = lds_u32_a2(blk + 96);                        // scales bytes 0..3
-  const uint32_t s_lo2 = lds_u32_a2(blk + 100);                      // scales bytes 4..7
-  const uint32_t s_hi = lds_u32_a2(blk + 104);                       // scales bytes 8..11
-  const uint32_t dbits = (uint32_t)blk[108] | ((uint32_t)blk[109] << 8);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(blk);
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+  const uint32_t sel = (a & 2u) ? 0x5432u : 0x3210u;  // block word i = prmt(w[i], w[i + 1], sel)
+  uint32_t hmw[5], qsw[5], scw[4];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) {
+    hmw[i] = w[4 * half + i];      // block words 4 half .. 4 half + 3: hmask bytes 16 half ..
+    qsw[i] = w[8 + 4 * c + i];     // block words 8 + 4c ..: quant bytes 32 + 16c ..
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) scw[i] = w[24 + i];  // block words 24 .. 26: scales; 27: d
+  uint32_t q[4], m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    q[i] = __byte_perm(qsw[i], qsw[i + 1], sel);
+    m[i] = __byte_perm(hmw[i], hmw[i + 1], sel);
+  }
+  const uint32_t s_lo = __byte_perm(scw[0], scw[1], sel);   // scales bytes 0..3
+  const uint32_t s_lo2 = __byte_perm(scw[1], scw[2], sel);  // scales bytes 4..7
+  const uint32_t s_hi = __byte_perm(scw[2], scw[3], sel);   // scales bytes 8..11
+  const uint32_t dbits = (a & 2u) ? (scw[3] >> 16) : (scw[3] & 0xFFFFu);
   float acc = 0.f;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t lmask = 0x03030303u << (2 * j);
     const uint32_t hmask = 0x01010101u << (4 * h + j);
-    int a = dp4a_us(q0 & lmask, x.q[4 * j + 0], 0);
-    a = dp4a_us(q1 & lmask, x.q[4 * j + 1], a);
-    a = dp4a_us(q2 & lmask, x.q[4 * j + 2], a);
-    a = dp4a_us(q3 & lmask, x.q[4 * j + 3], a);
-    int b = dp4a_us(m0 & hmask, x.q[4 * j + 0], 0);
-    b = dp4a_us(m1 & hmask, x.q[4 * j + 1], b);
-    b = dp4a_us(m2 & hmask, x.q[4 * j + 2], b);
-    b = dp4a_us(m3 & hmask, x.q[4 * j + 3], b);
-    const int isum = (a >> (2 * j)) + ((b >> (4 * h + j)) << 2) - 4 * x.s16[j];
+    int a0 = dp4a_us(q[0] & lmask, x.q[4 * j + 0], 0);
+    a0 = dp4a_us(q[1] & lmask, x.q[4 * j + 1], a0);
+    a0 = dp4a_us(q[2] & lmask, x.q[4 * j + 2], a0);
+    a0 = dp4a_us(q[3] & lmask, x.q[4 * j + 3], a0);
+    int b = dp4a_us(m[0] & hmask, x.q[4 * j + 0], 0);
+    b = dp4a_us(m[1] & hmask, x.q[4 * j + 1], b);
+    b = dp4a_us(m[2] & hmask, x.q[4 * j + 2], b);
+    b = dp4a_us(m[3] & hmask, x.q[4 * j + 3], b);
+    const int isum = (a0 >> (2 * j)) + ((b >> (4 * h + j)) << 2) - 4 * x.s16[j];
     // six-bit scale code of sub-block 8h + 2j + half
     const int sbyte = 2 * j + half;  // 0..7
     const uint32_t lo_src = sbyte < 4 ? s_lo : s_lo2;
