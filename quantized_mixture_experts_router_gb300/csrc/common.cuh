@@ -30,11 +30,14 @@ struct Ctrl {
   unsigned ticket;        // work tickets of the fused decode kernel
   unsigned q8_done;       // q8_1(x) tasks finished
   unsigned router_done;   // router tasks finished
-  unsigned reserved;
+  unsigned shdn_done;     // shared-expert down items finished (decode)
   unsigned shgu_done;     // shared-expert gate/up tasks finished
   unsigned rtgu_done;     // routed gate/up tasks finished
   unsigned exit_count;    // blocks that have left the fused kernel
-  unsigned pad[55];
+  unsigned ticket_sh;     // shared-expert down items taken (decode)
+  unsigned ticket_gu;     // routed gate/up items taken (decode)
+  unsigned ticket_dn;     // routed down items taken (decode)
+  unsigned pad[52];
 };
 
 // Routing of a decode call grouped by expert (ascending id), built in shared
@@ -358,12 +361,15 @@ __device__ __forceinline__ float q3k_unit_dot(const uint8_t* blk, int c, const X
 // 2^-19 max(|y|, 1) from every half-integer both round to the same integer.
 // Otherwise (a few values in 10^4), or when 1/d overflowed, the quotient is
 // computed exactly.
+// The exact quotient rule, out of line: it is taken for a few values in 10^4.
+static __device__ __noinline__ int q8_code_exact(float v, float d) { return (int)roundf(__fdiv_rn(v, d)); }
+
 __device__ __forceinline__ int q8_code(float v, float d, float rd) {
   const float y = v * rd;
   const float a = fabsf(y);
   const float f = a - floorf(a);
   if (a < 1.0e30f && fabsf(f - 0.5f) > 0x1.0p-19f * fmaxf(a, 1.0f)) return (int)copysignf(floorf(a + 0.5f), y);
-  return (int)roundf(__fdiv_rn(v, d));
+  return q8_code_exact(v, d);
 }
 
 // ------------------------------------------------------------------ q8_1 (warp)
@@ -418,43 +424,36 @@ __device__ __forceinline__ void q8_block_warp(float v, int qb, uint8_t* q8, int*
 // f32 operations in the same order for every value; amax and the integer sums
 // do not depend on the order.
 __device__ __forceinline__ void q8_block_thread(const uint16_t* x32, int qb, int* units) {
-  const uint4* xp = reinterpret_cast<const uint4*>(x32);
-  uint32_t raw[16];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 v = xp[i];
-    raw[4 * i + 0] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
-  }
+  const uint2* xp = reinterpret_cast<const uint2*>(x32);
   float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(raw[i])), fabsf(bf16hi(raw[i]))));
+#pragma unroll 1
+  for (int w = 0; w < 8; ++w) {
+    const uint2 v = xp[w];
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))), fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y)))));
+  }
   const float d = __fdiv_rn(amax, 127.0f);
   const float rd = __frcp_rn(d);
-  uint32_t word[8];
-  int s0 = 0, s1 = 0;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    uint32_t wd = 0;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int e = 4 * w + b;
-      const uint32_t r = raw[e >> 1];
-      const float v = (e & 1) ? bf16hi(r) : bf16lo(r);
-      const int q = amax == 0.0f ? 0 : q8_code(v, d, rd);
-      wd |= (uint32_t)(q & 0xFF) << (8 * b);
-      if (w < 4) s0 += q; else s1 += q;
-    }
-    word[w] = wd;
-  }
-  const float dq = __half2float(__float2half_rn(d));
   const int b256 = qb >> 3, hj = qb & 7, h = hj >> 2, j = hj & 3;
   int* u0 = units + ((size_t)b256 * 4 + 2 * h) * UNIT_WORDS;
-  int* u1 = u0 + UNIT_WORDS;
+  int s0 = 0, s1 = 0;
+  // words 0..3 of the block go to the first half unit, 4..7 to the second
+#pragma unroll 1
+  for (int w = 0; w < 8; ++w) {
+    const uint2 v = xp[w];
+    const float f[4] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y)};
+    uint32_t wd = 0;
+    int sw = 0;
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    u0[4 * j + w] = (int)word[w];
-    u1[4 * j + w] = (int)word[4 + w];
+    for (int b = 0; b < 4; ++b) {
+      const int q = amax == 0.0f ? 0 : q8_code(f[b], d, rd);
+      wd |= (uint32_t)(q & 0xFF) << (8 * b);
+      sw += q;
+    }
+    if (w < 4) s0 += sw; else s1 += sw;
+    u0[(w >> 2) * UNIT_WORDS + 4 * j + (w & 3)] = (int)wd;
   }
+  const float dq = __half2float(__float2half_rn(d));
+  int* u1 = u0 + UNIT_WORDS;
   u0[16 + j] = __float_as_int(dq);
   u1[16 + j] = __float_as_int(dq);
   u0[20 + j] = s0;

@@ -1,19 +1,23 @@
 // Decode path (m <= 8): one fused persistent kernel per layer call.
 //
-// One block per SM: a producer warp and NCW consumer warps around a ring of
-// NST shared-memory stages.  The producer takes ITEMS by ticket, in dependency
-// order
-//   q8_1(x) | router rows | shared gate/up | routed gate/up | down groups
-// and streams each item's raw weight rows into the ring as stages with 1-D
+// One block per SM: a producer warp, a planner warp and NCW consumer warps
+// around a ring of NST shared-memory stages.  The producer takes ITEMS by
+// ticket from four streams: first
+//   q8_1(x) | router rows | shared gate/up
+// then routed gate/up items as soon as its block's plan exists, shared down
+// items while it does not (and when the routed gate/up items run out), and
+// the routed down items last, and streams each item's raw weight rows into the ring as stages with 1-D
 // bulk copies (cp.async.bulk, completing on the stage's mbarrier).  Each stage
 // is one TASK, taken and finished by a single consumer warp; the warps of the
 // block share an item through a small shared-memory state (a task counter and
 // a result buffer), and the warp finishing an item's last task completes it:
-//   router item   -> counts it; after the last one, selection and the plan
+//   router item   -> counts it; the planner warp of every block then selects
+//                    the experts and groups the pairs into its own plan
 //   gate/up item  -> SwiGLU is done per task; the 32-row group of h goes to
 //                    q8_1 units (metrale's fused swiglu_q8 step)
-//   down item     -> y = sum over the picked experts in ascending id of
-//                    G_i E_i, then the shared expert, written to out
+//   shared down   -> y_shared of 8 output rows, written to out
+//   routed down   -> y = sum over the picked experts in ascending id of
+//                    G_i E_i, then + y_shared read back from out
 // so a device-scope fence is paid once per item, not per task.  Waits on
 // results of other blocks (q8_1(x), the plan, the h vectors) are bounded
 // spins; the producer never waits for results, so weight bytes keep
@@ -21,11 +25,21 @@
 // results do not depend on timing.  q8_1(x) and the h vectors are copied
 // into shared memory once per block (when they fit) with bulk copies.
 //
+// Code layout: the SM's instruction cache holds a few tens of KB, and warps
+// of one SM run different task kinds at once; a miss costs a trip to L2,
+// which under the full streaming load takes microseconds.  So every task kind
+// is one out-of-line routine with rolled loops, called from a single site,
+// the readiness of inputs is a block-level bit in shared memory, and every
+// block runs its routines once on scratch bytes right after its router rows
+// (the block-local item) so that they are cached before their phase.
+//
 // Method: DeepSeek V4.1 atlas "Mixture of experts" (Router, Routed expert and
 // Shared expert steps: g' = min(g, L), u' = clip(u, -L, L), h = g' sigmoid(g') u',
 // y = sum G_i E_i + y_shared); metrale moe_v41 module docs and moe_v41.rs
 // (Q2_K gate/up, Q3_K down, q8_1 activations, the shared expert added after
 // the routed experts).
+#include <algorithm>
+
 #include "internal.h"
 #include "select.cuh"
 
@@ -37,24 +51,33 @@ constexpr int NCW = 8;               // consumer warps
 constexpr int W_PROD = NCW;          // the producer warp
 constexpr int W_PLAN = NCW + 1;      // the planner warp: this block's copy of the routing
 constexpr int NTH = (NCW + 2) * 32;
-constexpr int SB = 20480;            // bytes per ring stage
-constexpr int NST = 8;               // ring stages
+constexpr int SB = 13440;            // bytes per ring stage (4 + 4 Q2_K rows of 5120)
+constexpr int NST = 12;              // ring stages: NCW in work plus the copies in flight
 constexpr int NIS = 4;               // item state slots
 constexpr int GR = 4;                // rows of W1 and of W3 per gate/up stage
 constexpr int GT = 32;               // rows per gate/up item (one q8_1 block of h)
 constexpr int DG = 8;                // output rows per down item
-constexpr int RR = 2;                // router rows per router item (one stage)
-constexpr int SHP = 8;               // shared bf16 (gate, up) row pairs per item
+constexpr int RR = 1;                // router rows per router item (one stage)
+constexpr int SHP = 8;               // shared bf16 (gate, up) row pairs per item, one row per stage
 constexpr int Q8B = 32;              // q8_1 blocks per q8 item (one per lane)
-constexpr int SDR = 4;               // shared bf16 down rows per stage
+constexpr int SDR = 2;               // shared bf16 down rows per stage
+constexpr int UB = UNIT_WORDS * 4;   // bytes of one activation unit
+// the producer ends the ring with one stop stage per consumer; a stop stage
+// is never released, so all of them must fit in the ring at once
+static_assert(NCW <= NST, "more consumer warps than ring stages");
+static_assert(GR == 4 && RR == 1 && SDR == 2, "the row routines are instantiated for these row counts");
+static_assert(SB % 16 == 0, "stages start on 16-byte boundaries");
 
-enum : int { K_STOP = 0, K_Q8, K_ROUTER, K_SHGU_B, K_GU_Q, K_DN_SHB, K_DN_SHQ, K_DN_RT };
-enum : int { I_Q8 = 0, I_ROUTER, I_SHGU_B, I_GU, I_DN };
+enum : int { K_STOP = 0, K_Q8, K_ROUTER, K_SHGU_B, K_GU_Q, K_DN_SHB, K_DN_SHQ, K_DN_RT, K_LOCAL };
+enum : int { I_Q8 = 0, I_ROUTER, I_SHGU_B, I_GU, I_SHDN, I_DN, I_LOCAL };
 // shared-memory copies: x (bf16), routed h units, shared h, q8_1(x) units, expert pointer table, bias
 enum : int { CB_XB = 0, CB_HR, CB_HS, CB_XU, CB_EP, CB_BIAS, N_CB };
+// block-level readiness of the inputs a task reads (bits of Ctl::rdy)
+enum : unsigned { RQ_XB = 1u, RQ_BIAS = 2u, RQ_XU = 4u, RQ_HR = 8u, RQ_HS = 16u, RQ_PLAN = 32u };
 
 struct Hdr {
   int kind, slot, a, b;
+  unsigned seq;  // the stage sequence number this header belongs to
 };
 
 struct Item {
@@ -71,7 +94,10 @@ struct Ctl {
   unsigned long long pbar;        // the block's plan is built
   unsigned long long cbar[N_CB];  // shared-memory copies: see CB_*
   unsigned cstate[N_CB];          // 0 empty, 1 being filled
-  unsigned next;               // consumer grab counter
+  unsigned next;                  // consumer grab counter
+  unsigned rdy;                   // RQ_* bits: inputs ready for every warp of the block
+  unsigned xq;                    // consumer warps done with their share of q8_1(x)
+  unsigned sink;                  // written only if a scratch pass returns an impossible value
 };
 
 __device__ __forceinline__ uint8_t* smem_base() {
@@ -83,6 +109,12 @@ __device__ __forceinline__ uint8_t* smem_base() {
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_cta(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.cta.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -109,7 +141,9 @@ struct Sizes {
 
 __device__ __forceinline__ Sizes sizes_of(const DecodeParams& p) {
   Sizes z;
-  z.n_q8 = (p.m * (p.D / 32) + Q8B - 1) / Q8B;
+  // with a shared-memory copy of q8_1(x) the planner warp of every block
+  // quantises x itself; otherwise q8 items write it to global memory
+  z.n_q8 = p.sm_x ? 0 : (p.m * (p.D / 32) + Q8B - 1) / Q8B;
   z.n_router = (p.N + RR - 1) / RR;
   z.shq = p.shared_kind != MOE_SHARED_BF16;
   z.gt = p.I / GT;
@@ -118,26 +152,33 @@ __device__ __forceinline__ Sizes sizes_of(const DecodeParams& p) {
   return z;
 }
 
-// Ticket -> item.  Items past the shared gate/up need n_exp; kind -1 asks
-// the caller to wait for the plan, kind -2 means no work is left.
-__device__ __forceinline__ Item decode_ticket(unsigned t, const Sizes& z, int groups, int n_exp) {
+// Ticket streams of the producer and the item a ticket stands for; kind -2
+// when the stream is exhausted.  The routed streams need n_exp >= 0.
+enum : int { S_MAIN = 0, S_SHDN, S_GU, S_DN, N_STREAMS };
+
+__device__ __forceinline__ Item decode_ticket(int stream, unsigned t, const Sizes& z, int groups, int n_exp) {
   Item it{-2, 0, 0, 0, 0};
-  if (t < (unsigned)z.n_q8) { it.kind = I_Q8; it.a = (int)t; return it; }
-  t -= z.n_q8;
-  if (t < (unsigned)z.n_router) { it.kind = I_ROUTER; it.a = (int)t; return it; }
-  t -= z.n_router;
-  if (t < (unsigned)z.n_shgu) {
-    if (z.shq) { it.kind = I_GU; it.a = -1; it.b = (int)t; }
-    else { it.kind = I_SHGU_B; it.a = (int)t; }
-    return it;
+  switch (stream) {
+    case S_MAIN:
+      if (t < (unsigned)z.n_q8) { it.kind = I_Q8; it.a = (int)t; return it; }
+      t -= z.n_q8;
+      if (t < (unsigned)z.n_router) { it.kind = I_ROUTER; it.a = (int)t; return it; }
+      t -= z.n_router;
+      if (t < (unsigned)z.n_shgu) {
+        if (z.shq) { it.kind = I_GU; it.a = -1; it.b = (int)t; }
+        else { it.kind = I_SHGU_B; it.a = (int)t; }
+      }
+      return it;
+    case S_SHDN:
+      if (t < (unsigned)groups) { it.kind = I_SHDN; it.a = (int)t; }
+      return it;
+    case S_GU:
+      if (t < (unsigned)(n_exp * z.gt)) { it.kind = I_GU; it.a = (int)(t / z.gt); it.b = (int)(t % z.gt); }
+      return it;
+    default:
+      if (n_exp > 0 && t < (unsigned)groups) { it.kind = I_DN; it.a = (int)t; }
+      return it;
   }
-  t -= z.n_shgu;
-  if (n_exp < 0) { it.kind = -1; return it; }
-  const unsigned n_rtgu = (unsigned)n_exp * z.gt;
-  if (t < n_rtgu) { it.kind = I_GU; it.a = (int)(t / z.gt); it.b = (int)(t % z.gt); return it; }
-  t -= n_rtgu;
-  if (t < (unsigned)groups) { it.kind = I_DN; it.a = (int)t; return it; }
-  return it;
 }
 
 // ---------------------------------------------------------- warp helpers
@@ -155,87 +196,195 @@ __device__ __forceinline__ void dot8(float2& acc, const uint4& w, const uint4& x
   acc.x = fmaf(bf16lo(w.w), bf16lo(x.w), acc.x); acc.y = fmaf(bf16hi(w.w), bf16hi(x.w), acc.y);
 }
 
-// an activation unit: from shared memory, or (written by other blocks in
-// this kernel) from L2 without the non-coherent read-only path
-__device__ __forceinline__ void load_unit(XUnit& x, const int4* p, bool in_smem) {
-  int4 v[6];
-  if (in_smem) {
+// 16 bytes of an activation vector: from the block's shared-memory copy (S,
+// byte offset so + off), else from global memory through L2 (the vector may
+// have been written by other blocks of this kernel)
+template <bool S>
+__device__ __forceinline__ uint4 vld(uint32_t so, const uint8_t* g, uint32_t off) {
+  if constexpr (S) return *reinterpret_cast<const uint4*>(smem_base() + so + off);
+  else return __ldcg(reinterpret_cast<const uint4*>(g + off));
+}
+
+template <bool S>
+__device__ __forceinline__ void load_unit(XUnit& x, uint32_t so, const uint8_t* g, uint32_t off) {
+  uint4 v[6];
 #pragma unroll
-    for (int i = 0; i < 6; ++i) v[i] = p[i];
-  } else {
+  for (int i = 0; i < 6; ++i) v[i] = vld<S>(so, g, off + 16u * i);
+  x.q[0] = (int)v[0].x; x.q[1] = (int)v[0].y; x.q[2] = (int)v[0].z; x.q[3] = (int)v[0].w;
+  x.q[4] = (int)v[1].x; x.q[5] = (int)v[1].y; x.q[6] = (int)v[1].z; x.q[7] = (int)v[1].w;
+  x.q[8] = (int)v[2].x; x.q[9] = (int)v[2].y; x.q[10] = (int)v[2].z; x.q[11] = (int)v[2].w;
+  x.q[12] = (int)v[3].x; x.q[13] = (int)v[3].y; x.q[14] = (int)v[3].z; x.q[15] = (int)v[3].w;
+  x.dq[0] = __uint_as_float(v[4].x); x.dq[1] = __uint_as_float(v[4].y);
+  x.dq[2] = __uint_as_float(v[4].z); x.dq[3] = __uint_as_float(v[4].w);
+  x.s16[0] = (int)v[5].x; x.s16[1] = (int)v[5].y; x.s16[2] = (int)v[5].z; x.s16[3] = (int)v[5].w;
+}
+
+// ------------------------------------------------------ row dot routines
+// R rows of bf16 weights (stage offset w, row stride rs bytes) dotted with
+// one bf16 vector of `chunks` 16-byte chunks (chunks a multiple of 32).
+// Every lane returns the R sums.
+template <int R, bool S>
+__device__ __noinline__ float4 bf16_rows_dot(uint32_t w, uint32_t rs, uint32_t vs, const uint8_t* vg, int chunks) {
+  const int lane = threadIdx.x & 31;
+  const uint8_t* sw = smem_base() + w;
+  float2 a[R], b[R];
 #pragma unroll
-    for (int i = 0; i < 6; ++i) v[i] = __ldcg(p + i);
-  }
-  x.q[0] = v[0].x; x.q[1] = v[0].y; x.q[2] = v[0].z; x.q[3] = v[0].w;
-  x.q[4] = v[1].x; x.q[5] = v[1].y; x.q[6] = v[1].z; x.q[7] = v[1].w;
-  x.q[8] = v[2].x; x.q[9] = v[2].y; x.q[10] = v[2].z; x.q[11] = v[2].w;
-  x.q[12] = v[3].x; x.q[13] = v[3].y; x.q[14] = v[3].z; x.q[15] = v[3].w;
-  x.dq[0] = __int_as_float(v[4].x); x.dq[1] = __int_as_float(v[4].y);
-  x.dq[2] = __int_as_float(v[4].z); x.dq[3] = __int_as_float(v[4].w);
-  x.s16[0] = v[5].x; x.s16[1] = v[5].y; x.s16[2] = v[5].z; x.s16[3] = v[5].w;
-}
-
-// ------------------------------------------------------------- context
-struct Ctx {
-  const DecodeParams& p;
-  const Sizes& z;
-  Ctl& C;
-  uint64_t deadline;
-  int n_exp;  // -1 until the warp has read the plan
-  bool x_ok, rt_ok, sh_ok, plan_ok, xb_ok;
-};
-
-// Wait (once per warp) for the copy of x that the producer started at launch.
-__device__ __forceinline__ void need_xb(Ctx& c) {
-  if (c.p.sm_xb && !c.xb_ok) {
-    if ((threadIdx.x & 31) == 0) mbar_wait_bounded(bar(c.C.cbar[CB_XB]), 0u, c.deadline, &c.p.ctrl->status);
-    __syncwarp();
-    c.xb_ok = true;
-  }
-}
-
-// The block's shared-memory copy of the plan (bulk-copied by the producer once
-// the plan exists); the first use by a warp waits for the copy.
-__device__ __forceinline__ const DecodePlan* splan(Ctx& c) {
-  if (!c.plan_ok) {
-    if ((threadIdx.x & 31) == 0) mbar_wait_bounded(bar(c.C.pbar), 0u, c.deadline, &c.p.ctrl->status);
-    __syncwarp();
-    c.plan_ok = true;
-  }
-  return reinterpret_cast<const DecodePlan*>(smem_base() + c.p.sm_plan);
-}
-
-__device__ __forceinline__ int plan_n_exp(Ctx& c) {
-  if (c.n_exp < 0) c.n_exp = splan(c)->n_exp;
-  return c.n_exp;
-}
-
-// Bounded wait of a whole warp on a global counter (lane 0 spins).
-__device__ __forceinline__ bool warp_wait(Ctx& c, bool& done_flag, const unsigned* ctr, unsigned target) {
-  if (!done_flag) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = wait_count(ctr, target, c.deadline, &c.p.ctrl->status);
-    done_flag = __shfl_sync(0xffffffffu, ok, 0);
-  }
-  return done_flag;
-}
-
-// Shared-memory copy of a region written by other blocks, made once per block
-// (which = CB_HR, CB_HS or CB_XU).  The first warp to need it
-// waits for the producing counter, then bulk-copies it; every warp waits on
-// the copy's mbarrier.
-__device__ void ensure_cache(Ctx& c, int which, const unsigned* counter, unsigned target, const void* src,
-                             uint32_t bytes, uint32_t dst_off) {
-  if ((threadIdx.x & 31) == 0) {
-    if (atomicCAS(&c.C.cstate[which], 0u, 1u) == 0u) {
-      wait_count(counter, target, c.deadline, &c.p.ctrl->status);
-      asm volatile("fence.proxy.async;" ::: "memory");
-      mbar_arrive_expect_tx(bar(c.C.cbar[which]), bytes);
-      bulk_g2s(smem_base() + dst_off, src, bytes, bar(c.C.cbar[which]));
+  for (int r = 0; r < R; ++r) a[r] = b[r] = make_float2(0.f, 0.f);
+#pragma unroll 1
+  for (int ch = lane; ch < chunks; ch += 64) {
+    const uint4 v0 = vld<S>(vs, vg, 16u * ch);
+#pragma unroll
+    for (int r = 0; r < R; ++r) dot8(a[r], *reinterpret_cast<const uint4*>(sw + r * rs + 16u * ch), v0);
+    if (ch + 32 < chunks) {
+      const uint4 v1 = vld<S>(vs, vg, 16u * (ch + 32));
+#pragma unroll
+      for (int r = 0; r < R; ++r) dot8(b[r], *reinterpret_cast<const uint4*>(sw + r * rs + 16u * (ch + 32)), v1);
     }
-    mbar_wait_bounded(bar(c.C.cbar[which]), 0u, c.deadline, &c.p.ctrl->status);
+  }
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < R; ++r) o[r] = warp_sum((a[r].x + a[r].y) + (b[r].x + b[r].y));
+  return make_float4(o[0], o[1], o[2], o[3]);
+}
+
+// Four Q2_K rows (stage offset w, row stride rb) against one q8_1(x) vector
+// in the unit layout, by a half-warp (16 lanes, 1/16 of the units each).
+// Every lane of the half returns the four sums.
+template <bool S>
+__device__ __noinline__ float4 q2k_rows4_dot(uint32_t w, uint32_t rb, int U, uint32_t xs, const uint8_t* xg) {
+  const int l = threadIdx.x & 15;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 1
+  for (int u = l; u < U; u += 16) {
+    XUnit xr;
+    load_unit<S>(xr, xs, xg, (uint32_t)u * UB);
+    const uint8_t* blk = smem_base() + w + (u >> 2) * Q2K_B;
+    const int c = u & 3;
+    a0 += q2k_unit_dot(blk, c, xr);
+    a1 += q2k_unit_dot(blk + rb, c, xr);
+    a2 += q2k_unit_dot(blk + 2 * rb, c, xr);
+    a3 += q2k_unit_dot(blk + 3 * rb, c, xr);
+  }
+#pragma unroll
+  for (int o = 8; o; o >>= 1) {
+    a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+    a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+    a3 += __shfl_xor_sync(0xffffffffu, a3, o);
+  }
+  return make_float4(a0, a1, a2, a3);
+}
+
+// One Q3_K row (stage offset rowp) against one q8_1(h) vector, by the four
+// lanes of a row group (1/4 of the units each); the four lanes return the sum.
+template <bool S>
+__device__ __noinline__ float q3k_row_dot(uint32_t rowp, int U2, uint32_t hs, const uint8_t* hg) {
+  const int q = threadIdx.x & 3;
+  float acc = 0.f;
+#pragma unroll 1
+  for (int u = q; u < U2; u += 4) {
+    XUnit hr;
+    load_unit<S>(hr, hs, hg, (uint32_t)u * UB);
+    acc += q3k_unit_dot(smem_base() + rowp + (u >> 2) * Q3K_B, u & 3, hr);
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  return acc;
+}
+
+// ------------------------------------------------------------- readiness
+// Copy of a region written by other blocks into shared memory, made once per
+// block: the first warp to need it waits for the producing counter, then
+// bulk-copies it; every warp waits on the copy's mbarrier.  Without a copy
+// (dst 0) the counter itself is waited for.  Lane 0 only.
+__device__ void fill_or_wait(Ctl& C, int which, const unsigned* counter, unsigned target, const void* src,
+                             uint32_t bytes, uint32_t dst, uint64_t deadline, unsigned* status) {
+  if (!dst) {
+    wait_count(counter, target, deadline, status);
+    return;
+  }
+  if (atomicCAS(&C.cstate[which], 0u, 1u) == 0u) {
+    wait_count(counter, target, deadline, status);
+    asm volatile("fence.proxy.async;" ::: "memory");
+    mbar_arrive_expect_tx(bar(C.cbar[which]), bytes);
+    bulk_g2s(smem_base() + dst, src, bytes, bar(C.cbar[which]));
+  }
+  mbar_wait_bounded(bar(C.cbar[which]), 0u, deadline, status);
+}
+
+// Returns once the inputs in `bits` (RQ_*) are ready.  The first warp of the
+// block to need one waits for it and publishes the bit (release at block
+// scope after its own acquire), so later warps pay one shared-memory load.
+// After a timeout the bit is published anyway (the status word says why).
+__device__ __noinline__ void require(const DecodeParams& p, Ctl& C, unsigned bits, uint64_t deadline) {
+  if ((threadIdx.x & 31) == 0) {
+    const unsigned have = ld_acquire_cta(&C.rdy);
+    unsigned need = bits & ~have;
+    unsigned* st = &p.ctrl->status;
+    while (need) {
+      const unsigned bit = need & (0u - need);
+      need &= need - 1u;
+      const Sizes z = sizes_of(p);
+      switch (bit) {
+        case RQ_XB:
+          if (p.sm_xb) mbar_wait_bounded(bar(C.cbar[CB_XB]), 0u, deadline, st);
+          break;
+        case RQ_BIAS:
+          if (p.sm_bias) mbar_wait_bounded(bar(C.cbar[CB_BIAS]), 0u, deadline, st);
+          break;
+        case RQ_PLAN:
+          mbar_wait_bounded(bar(C.pbar), 0u, deadline, st);
+          break;
+        case RQ_XU:
+          if (p.sm_x) {
+            // every consumer warp quantises its share of x at launch
+            uint32_t spins = 0;
+            while (ld_acquire_cta(&C.xq) < (unsigned)NCW) {
+              __nanosleep(64);
+              if ((++spins & 15u) == 0 && globaltimer_ns() > deadline) {
+                atomicOr(st, (unsigned)MOE_STATUS_TIMEOUT);
+                break;
+              }
+            }
+          } else {
+            wait_count(&p.ctrl->q8_done, (unsigned)z.n_q8, deadline, st);
+          }
+          break;
+        case RQ_HR: {
+          mbar_wait_bounded(bar(C.pbar), 0u, deadline, st);
+          const DecodePlan* plan = reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan);
+          fill_or_wait(C, CB_HR, &p.ctrl->rtgu_done, (unsigned)(plan->n_exp * z.gt), p.hu,
+                       (uint32_t)(p.m * p.k * unit_bytes(p.I)), p.sm_hr, deadline, st);
+          break;
+        }
+        case RQ_HS:
+          if (z.shq)
+            fill_or_wait(C, CB_HS, &p.ctrl->shgu_done, (unsigned)z.n_shgu,
+                         p.hu + (size_t)p.shvec0 * (unit_bytes(p.I) / 4), (uint32_t)(p.m * unit_bytes(p.I)), p.sm_hs,
+                         deadline, st);
+          else
+            fill_or_wait(C, CB_HS, &p.ctrl->shgu_done, (unsigned)z.n_shgu, p.shh, (uint32_t)(p.m * 2 * p.I),
+                         p.sm_hs, deadline, st);
+          break;
+        default:
+          break;
+      }
+      __threadfence_block();
+      atomicOr(&C.rdy, bit);
+    }
   }
   __syncwarp();
+}
+
+__host__ __device__ __forceinline__ size_t a16d(size_t v) { return (v + 15) & ~size_t(15); }
+
+// the selection scratch, picks and sorted pairs, then the plan
+__host__ __device__ __forceinline__ size_t plan_scratch_bytes(int N) {
+  return a16d(select_scratch_bytes(N) + (size_t)4 * MAXP * 4) + sizeof(DecodePlan);
+}
+
+__device__ __forceinline__ const DecodePlan* plan_of(const DecodeParams& p) {
+  return reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan);
 }
 
 // ------------------------------------------------------------- the plan
@@ -245,34 +394,39 @@ __device__ void ensure_cache(Ctx& c, int which, const unsigned* counter, unsigne
 // computes the same plan; block 0 also writes the routing outputs).  Under
 // full load every dependent global round trip costs microseconds, so the
 // plan never goes through global memory.
-__device__ void build_plan(Ctx& c) {
-  const DecodeParams& p = c.p;
+// sel, plan: shared-memory offsets of the selection scratch and of the plan.
+// dry: a run on scratch space only (the block-local item's cache warm-up),
+// which writes nothing outside shared memory and leaves the status alone.
+__device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t deadline, uint32_t sel,
+                                        uint32_t plan_off, bool dry) {
   const int lane = threadIdx.x & 31;
-  float* scratch = reinterpret_cast<float*>(smem_base() + p.sm_sel);
-  int* pk_id = reinterpret_cast<int*>(smem_base() + p.sm_sel + select_scratch_bytes(p.N));
+  float* scratch = reinterpret_cast<float*>(smem_base() + sel);
+  int* pk_id = reinterpret_cast<int*>(smem_base() + sel + select_scratch_bytes(p.N));
   float* pk_w = reinterpret_cast<float*>(pk_id + MAXP);
   int* s_e = pk_id + 2 * MAXP;  // expert of each sorted position
   int* s_t = pk_id + 3 * MAXP;  // token of each sorted position
-  const bool writer = blockIdx.x == 0;
+  const bool writer = blockIdx.x == 0 && !dry;
+  unsigned* status = dry ? &C.sink : &p.ctrl->status;
+#pragma unroll 1
   for (int t = 0; t < p.m; ++t) {
     float* wo = writer ? p.topk_w + (size_t)t * p.k : pk_w + t * p.k;
     int* io = writer ? p.topk_idx + (size_t)t * p.k : pk_id + t * p.k;
     if (p.N <= 384)
       route_token_warp_r12(p.logits + (size_t)t * p.N, p.sk + (size_t)t * p.N, p.bias, p.N, p.k, p.gate_temp,
-                           p.norm, p.route_scale, wo, io, &p.ctrl->status, scratch, pk_id + t * p.k, pk_w + t * p.k);
+                           p.norm, p.route_scale, wo, io, status, scratch, pk_id + t * p.k, pk_w + t * p.k);
     else
       route_token_warp(p.logits + (size_t)t * p.N, p.sk + (size_t)t * p.N, p.bias, p.N, p.k, p.gate_temp, p.norm,
-                       p.route_scale, wo, io, &p.ctrl->status, scratch, pk_id + t * p.k, pk_w + t * p.k);
+                       p.route_scale, wo, io, status, scratch, pk_id + t * p.k, pk_w + t * p.k);
   }
   // the expert pointer table: the block's copy when there is one
   const unsigned long long* eptr = p.expert_ptrs;
   if (p.ep_bytes) {
-    mbar_wait_bounded(bar(c.C.cbar[CB_EP]), 0u, c.deadline, &p.ctrl->status);
+    mbar_wait_bounded(bar(C.cbar[CB_EP]), 0u, deadline, &p.ctrl->status);
     __syncwarp();
   }
   const unsigned long long* eptr_s = reinterpret_cast<const unsigned long long*>(smem_base() + p.sm_ep);
   __syncwarp();
-  DecodePlan* plan = reinterpret_cast<DecodePlan*>(smem_base() + p.sm_plan);
+  DecodePlan* plan = reinterpret_cast<DecodePlan*>(smem_base() + plan_off);
   const int P = p.m * p.k;
   for (int i = lane; i < P; i += 32) {
     const int e = pk_id[i], t = i / p.k;
@@ -304,7 +458,7 @@ __device__ void build_plan(Ctx& c) {
         ptr[j] = (w + 1) * 8 <= p.ep_bytes ? eptr_s[w] : eptr[w];
       }
       for (int j = 0; j < 3; ++j) bad |= (ptr[j] == 0ull) || (ptr[j] & 255ull);
-      if (bad && writer) atomicOr(&p.ctrl->status, (unsigned)MOE_STATUS_MISSING_EXPERT);
+      if (bad && writer) atomicOr(status, (unsigned)MOE_STATUS_MISSING_EXPERT);
       for (int j = 0; j < 3; ++j) plan->exp_ptr[slot][j] = bad ? 0ull : ptr[j];
     }
     n_exp += __popc(bal);
@@ -330,222 +484,196 @@ __device__ __forceinline__ float* item_buf(const DecodeParams& p, int slot) {
 }
 
 // q8_1 of x into global units: Q8B of the m*D/32 blocks, one per thread
-__device__ void task_q8(Ctx& c, int it) {
-  const DecodeParams& p = c.p;
+__device__ __noinline__ void task_q8(const DecodeParams& p, int it) {
   const int lane = threadIdx.x & 31;
   const int nb = p.D / 32;
   const int total = p.m * nb;
-  for (int g = it * Q8B + lane; g < it * Q8B + Q8B && g < total; g += 32) {
+  const int g = it * Q8B + lane;
+  if (g < total) {
     const int t = g / nb, qb = g % nb;
     q8_block_thread(p.x + (size_t)t * p.D + (size_t)qb * 32, qb, p.xu + (size_t)t * (unit_bytes(p.D) / 4));
   }
 }
 
-// x of token t as uint4 chunks: the shared-memory copy when there is one
-__device__ __forceinline__ uint4 x_chunk(const DecodeParams& p, int t, int ch) {
-  if (p.sm_xb) return reinterpret_cast<const uint4*>(smem_base() + p.sm_xb)[(size_t)t * (p.D / 8) + ch];
-  return __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.D) + ch);
+// q8_1 of x into the block's shared-memory unit layout: q8_1 blocks first,
+// first + stride, ... of all tokens, one per thread
+__device__ __noinline__ void quantize_x_smem(const DecodeParams& p, int first, int stride) {
+  const int nb = p.D / 32;
+  const uint16_t* xs = p.sm_xb ? reinterpret_cast<const uint16_t*>(smem_base() + p.sm_xb) : p.x;
+#pragma unroll 1
+  for (int g = first; g < p.m * nb; g += stride) {
+    const int t = g / nb, qb = g % nb;
+    q8_block_thread(xs + (size_t)t * p.D + (size_t)qb * 32, qb,
+                    reinterpret_cast<int*>(smem_base() + p.sm_x + (size_t)t * unit_bytes(p.D)));
+  }
 }
 
-// router rows r0, r0+1 against every token -> logits
-__device__ void task_router(Ctx& c, const uint8_t* stage, int r0) {
-  const DecodeParams& p = c.p;
+// Block-local work, NCW tasks per block issued after the block's router rows:
+// share `part` of q8_1(x) into shared memory, and one pass of a row routine
+// on scratch bytes of the ring (results discarded) so that the routines the
+// later phases run are already in the instruction cache.
+__device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t deadline, uint32_t sel,
+                                        uint32_t plan_off, bool dry);
+
+// (Part NCW/2 instead runs the selection and the plan builder dry, on its own
+// stage as scratch, for the planner warp that runs them for real later.)
+__device__ __noinline__ void task_local(const DecodeParams& p, Ctl& C, uint32_t st, int part, uint64_t deadline) {
   const int lane = threadIdx.x & 31;
-  const int chunks = p.D / 8;
-  const uint4* w = reinterpret_cast<const uint4*>(stage);
-  const int rows = min(RR, p.N - r0);
-  need_xb(c);
-  if (p.sm_bias && (threadIdx.x & 31) == 0) mbar_wait_bounded(bar(c.C.cbar[CB_BIAS]), 0u, c.deadline, &p.ctrl->status);
-  __syncwarp();
+  if (p.sm_x) {
+    require(p, C, RQ_XB, deadline);
+    quantize_x_smem(p, part * 32 + lane, NCW * 32);
+    __syncwarp();
+    __threadfence_block();
+    if (lane == 0) atomicAdd(&C.xq, 1u);
+  }
+  if (part == NCW / 2 && plan_scratch_bytes(p.N) <= (size_t)SB) {
+    build_plan(p, C, deadline, st, st + (uint32_t)a16d(select_scratch_bytes(p.N) + (size_t)4 * MAXP * 4), true);
+    return;
+  }
+  float sink = 0.f;
+  const uint32_t sv = (uint32_t)SB;  // scratch bytes of stage 1
+  switch (part & 3) {
+    case 0: sink = bf16_rows_dot<1, true>(0u, 0u, sv, nullptr, min(p.D / 8, 256)).x; break;
+    case 1: sink = bf16_rows_dot<2, true>(0u, 2u * p.I, sv, nullptr, min(p.I / 8, 256)).x; break;
+    case 2: sink = q2k_rows4_dot<true>(0u, (p.D / QK) * Q2K_B, min(p.D / 64, 64), sv, nullptr).x; break;
+    default:
+      sink = q3k_row_dot<true>((uint32_t)((lane >> 2) * (p.I / QK) * Q3K_B), min(p.I / 64, 64), sv, nullptr);
+      break;
+  }
+  if (sink == 1.2345678e-30f) C.sink = 1u;
+}
+
+// router row e (stage offset st) against every token -> the logit and the
+// fast (score, key) pair the selection starts from
+__device__ __noinline__ void task_router(const DecodeParams& p, Ctl& C, uint32_t st, int e, uint64_t deadline) {
+  const int lane = threadIdx.x & 31;
+  require(p, C, RQ_XB | RQ_BIAS, deadline);
   const float* bias = p.sm_bias ? reinterpret_cast<const float*>(smem_base() + p.sm_bias) : p.bias;
+#pragma unroll 1
   for (int t = 0; t < p.m; ++t) {
-    float2 a0[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, a1[2] = {a0[0], a0[0]};
-    for (int ch = lane, i = 0; ch < chunks; ch += 32, ++i) {
-      const uint4 xv = x_chunk(p, t, ch);
-      dot8(a0[i & 1], w[ch], xv);
-      if (rows > 1) dot8(a1[i & 1], w[chunks + ch], xv);
-    }
-    const float s0 = warp_sum((a0[0].x + a0[0].y) + (a0[1].x + a0[1].y));
-    const float s1 = warp_sum((a1[0].x + a1[0].y) + (a1[1].x + a1[1].y));
-    // the logit, and the fast score and key the selection starts from
-    if (lane < rows) {
-      const float z = lane == 0 ? s0 : s1;
-      const int e = r0 + lane;
-      const float sc = score_fast(z, p.gate_temp);
-      p.logits[(size_t)t * p.N + e] = z;
+    const float4 s = p.sm_xb ? bf16_rows_dot<1, true>(st, 0u, p.sm_xb + 2u * t * p.D, nullptr, p.D / 8)
+                             : bf16_rows_dot<1, false>(st, 0u, 0u,
+                                                       reinterpret_cast<const uint8_t*>(p.x + (size_t)t * p.D), p.D / 8);
+    if (lane == 0) {
+      const float sc = score_fast(s.x, p.gate_temp);
+      p.logits[(size_t)t * p.N + e] = s.x;
       p.sk[(size_t)t * p.N + e] = make_float2(sc, __fadd_rn(sc, bias[e]));
     }
   }
 }
 
-// one (gate, up) row pair of the bf16 shared expert: h = SwiGLU(g, u) -> bf16
-__device__ void task_shgu_b(Ctx& c, const uint8_t* stage, int row) {
-  const DecodeParams& p = c.p;
+// one gate (which 0) or up (which 1) row of the bf16 shared expert against
+// every token -> item buffer slot (pair s of the item, which, token); the
+// item's completion applies SwiGLU
+__device__ __noinline__ void task_shgu_b(const DecodeParams& p, Ctl& C, uint32_t st, int s, int which, float* ib,
+                                         uint64_t deadline) {
   const int lane = threadIdx.x & 31;
-  const int chunks = p.D / 8;
-  const uint4* w = reinterpret_cast<const uint4*>(stage);
-  need_xb(c);
+  require(p, C, RQ_XB, deadline);
+#pragma unroll 1
   for (int t = 0; t < p.m; ++t) {
-    float2 ga[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, ua[2] = {ga[0], ga[0]};
-    for (int ch = lane, i = 0; ch < chunks; ch += 32, ++i) {
-      const uint4 xv = x_chunk(p, t, ch);
-      dot8(ga[i & 1], w[ch], xv);
-      dot8(ua[i & 1], w[chunks + ch], xv);
-    }
-    const float g = warp_sum((ga[0].x + ga[0].y) + (ga[1].x + ga[1].y));
-    const float u = warp_sum((ua[0].x + ua[0].y) + (ua[1].x + ua[1].y));
-    if (lane == 0)
-      reinterpret_cast<__nv_bfloat16*>(p.shh)[(size_t)t * p.I + row] =
-          __float2bfloat16_rn(swiglu_f32(g, u, p.swiglu_limit));
+    const float4 r = p.sm_xb ? bf16_rows_dot<1, true>(st, 0u, p.sm_xb + 2u * t * p.D, nullptr, p.D / 8)
+                             : bf16_rows_dot<1, false>(st, 0u, 0u,
+                                                       reinterpret_cast<const uint8_t*>(p.x + (size_t)t * p.D), p.D / 8);
+    if (lane == 0) ib[(size_t)(2 * s + which) * p.m + t] = r.x;
   }
 }
 
 // GR rows of W1 (stage offset 0) and of W3 (offset GR*rb) in Q2_K against the
-// q8_1(x) units of the item's tokens: half-warp 0 takes W1, half-warp 1 W3,
-// each lane 1/16 of the units of every row.  h of the rows -> item buffer.
-__device__ void task_gu_q(Ctx& c, const uint8_t* stage, int slot, int stg, float* ib) {
-  const DecodeParams& p = c.p;
-  const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
-  const int rb = (p.D / QK) * Q2K_B;
+// q8_1(x) units of the item's tokens: half-warp 0 takes W1, half-warp 1 W3.
+// h of the rows -> item buffer.
+__device__ __noinline__ void task_gu_q(const DecodeParams& p, Ctl& C, uint32_t st, int slot, int stg, float* ib,
+                                       uint64_t deadline) {
+  const int lane = threadIdx.x & 31, half = lane >> 4;
+  const uint32_t rb = (p.D / QK) * Q2K_B;
   const int U = p.D / 64;
   const bool shared = slot < 0;
   int pair0 = 0, ntok = p.m;
-  const DecodePlan* plan = shared ? nullptr : splan(c);
+  const DecodePlan* plan = plan_of(p);
   if (!shared) {
+    require(p, C, RQ_PLAN, deadline);
     pair0 = plan->exp_off[slot];
     ntok = plan->exp_off[slot + 1] - pair0;
     if (plan->exp_ptr[slot][0] == 0ull) return;
   }
-  const bool xs = p.sm_x != 0;
-  if (xs) ensure_cache(c, CB_XU, &p.ctrl->q8_done, (unsigned)c.z.n_q8, p.xu, (uint32_t)(p.m * unit_bytes(p.D)), p.sm_x);
-  else warp_wait(c, c.x_ok, &p.ctrl->q8_done, (unsigned)c.z.n_q8);
-  const uint8_t* base = stage + (size_t)half * GR * rb;
-  const size_t xstride = unit_bytes(p.D) / 16;
-  const int4* xall = xs ? reinterpret_cast<const int4*>(smem_base() + p.sm_x) : reinterpret_cast<const int4*>(p.xu);
+  require(p, C, RQ_XU, deadline);
+  const uint32_t w = st + (uint32_t)half * GR * rb;
+  const uint32_t xstride = unit_bytes(p.D);
+#pragma unroll 1
   for (int tt = 0; tt < ntok; ++tt) {
     const int tok = shared ? tt : plan->pair_tok[pair0 + tt];
-    const int4* xb = xall + (size_t)tok * xstride;
-    float acc[GR];
-#pragma unroll
-    for (int r = 0; r < GR; ++r) acc[r] = 0.f;
-    for (int u = l; u < U; u += 16) {
-      XUnit xr;
-      load_unit(xr, xb + u * 6, xs);
-      const uint8_t* ub = base + (u >> 2) * Q2K_B;
-#pragma unroll
-      for (int r = 0; r < GR; ++r) acc[r] += q2k_unit_dot(ub + (size_t)r * rb, u & 3, xr);
-    }
-#pragma unroll
-    for (int r = 0; r < GR; ++r) {
-#pragma unroll
-      for (int o = 8; o; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
-    }
-    // lane 0 holds g, lane 16 holds u
-#pragma unroll
-    for (int r = 0; r < GR; ++r) {
-      const float u = __shfl_sync(0xffffffffu, acc[r], 16);
-      if (lane == 0) ib[(stg * GR + r) * p.m + tt] = swiglu_f32(acc[r], u, p.swiglu_limit);
+    const float4 a = p.sm_x ? q2k_rows4_dot<true>(w, rb, U, p.sm_x + (uint32_t)tok * xstride, nullptr)
+                            : q2k_rows4_dot<false>(w, rb, U, 0u,
+                                                   reinterpret_cast<const uint8_t*>(p.xu) + (size_t)tok * xstride);
+    // lanes 0..15 hold the W1 sums, lanes 16..31 the W3 sums
+    const float u0 = __shfl_sync(0xffffffffu, a.x, 16), u1 = __shfl_sync(0xffffffffu, a.y, 16);
+    const float u2 = __shfl_sync(0xffffffffu, a.z, 16), u3 = __shfl_sync(0xffffffffu, a.w, 16);
+    if (lane == 0) {
+      float* o = ib + (size_t)stg * GR * p.m + tt;
+      o[0] = swiglu_f32(a.x, u0, p.swiglu_limit);
+      o[p.m] = swiglu_f32(a.y, u1, p.swiglu_limit);
+      o[2 * p.m] = swiglu_f32(a.z, u2, p.swiglu_limit);
+      o[3 * p.m] = swiglu_f32(a.w, u3, p.swiglu_limit);
     }
   }
 }
 
-// 8 rows of a Q3_K down matrix (stage) against h units: lane = (row, 1/4 of
-// the units).  Routed: E of each pair of the slot -> item buffer (unweighted);
-// shared (slot < 0): the shared expert's rows.
-__device__ void task_dn_q(Ctx& c, const uint8_t* stage, int slot, float* ib) {
-  const DecodeParams& p = c.p;
+// DG rows of a Q3_K down matrix (stage offset st) against h units: lane =
+// (row, 1/4 of the units).  Routed (slot >= 0): E of each pair of the slot ->
+// item buffer row pair*DG (unweighted); shared (slot < 0): the shared
+// expert's rows -> item buffer row t*DG.
+__device__ __noinline__ void task_dn_q(const DecodeParams& p, Ctl& C, uint32_t st, int slot, float* ib,
+                                       uint64_t deadline) {
   const int lane = threadIdx.x & 31, row = lane >> 2, q = lane & 3;
-  const int rb2 = (p.I / QK) * Q3K_B;
+  const uint32_t rb2 = (p.I / QK) * Q3K_B;
   const int U2 = p.I / 64;
-  const bool shared = slot < 0;
-  const int P = p.m * p.k;
-  const size_t hstride = unit_bytes(p.I) / 16;
+  const uint32_t hstride = unit_bytes(p.I);
   int pb = 0, pe = p.m;
-  bool present = true, hs;
-  const int4* hbase;
-  if (!shared) {
-    const DecodePlan* plan = splan(c);
+  bool present = true;
+  uint32_t hs;
+  const uint8_t* hg;
+  if (slot >= 0) {
+    require(p, C, RQ_PLAN | RQ_HR, deadline);
+    const DecodePlan* plan = plan_of(p);
     pb = plan->exp_off[slot];
     pe = plan->exp_off[slot + 1];
     present = plan->exp_ptr[slot][2] != 0ull;
-    const unsigned target = (unsigned)(plan_n_exp(c) * c.z.gt);
-    hs = p.sm_hr != 0;
-    if (hs) {
-      ensure_cache(c, CB_HR, &p.ctrl->rtgu_done, target, p.hu, (uint32_t)(P * unit_bytes(p.I)), p.sm_hr);
-      hbase = reinterpret_cast<const int4*>(smem_base() + p.sm_hr);
-    } else {
-      warp_wait(c, c.rt_ok, &p.ctrl->rtgu_done, target);
-      hbase = reinterpret_cast<const int4*>(p.hu);
-    }
+    hs = p.sm_hr;
+    hg = reinterpret_cast<const uint8_t*>(p.hu);
   } else {
-    hs = p.sm_hs != 0;
-    const unsigned target = (unsigned)c.z.n_shgu;
-    if (hs) {
-      ensure_cache(c, CB_HS, &p.ctrl->shgu_done, target, p.hu + (size_t)p.shvec0 * (unit_bytes(p.I) / 4),
-                   (uint32_t)(p.m * unit_bytes(p.I)), p.sm_hs);
-      hbase = reinterpret_cast<const int4*>(smem_base() + p.sm_hs);
-    } else {
-      warp_wait(c, c.sh_ok, &p.ctrl->shgu_done, target);
-      hbase = reinterpret_cast<const int4*>(p.hu) + (size_t)p.shvec0 * hstride;
-    }
+    require(p, C, RQ_HS, deadline);
+    hs = p.sm_hs;
+    hg = reinterpret_cast<const uint8_t*>(p.hu) + (size_t)p.shvec0 * hstride;
   }
-  const uint8_t* rowp = stage + (size_t)row * rb2;
+  const uint32_t rowp = st + (uint32_t)row * rb2;
+#pragma unroll 1
   for (int pi = pb; pi < pe; ++pi) {
+    const int v = slot >= 0 ? pi : pi - pb;  // vector index within the source
     float acc = 0.f;
-    if (present) {
-      const int4* hb = hbase + (size_t)pi * hstride;
-      for (int u = q; u < U2; u += 4) {
-        XUnit hr;
-        load_unit(hr, hb + u * 6, hs);
-        acc += q3k_unit_dot(rowp + (u >> 2) * Q3K_B, u & 3, hr);
-      }
-    }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    if (q == 0) {
-      if (shared) ib[(P + pi) * DG + row] = acc;
-      else ib[pi * DG + row] = acc;
-    }
+    if (present)
+      acc = hs ? q3k_row_dot<true>(rowp, U2, hs + (uint32_t)v * hstride, nullptr)
+               : q3k_row_dot<false>(rowp, U2, 0u, hg + (size_t)v * hstride);
+    if (q == 0) ib[(size_t)pi * DG + row] = acc;
   }
 }
 
 // SDR rows of the bf16 shared down matrix against h (bf16 [m, I]) -> item buffer
-__device__ void task_dn_b(Ctx& c, const uint8_t* stage, int part, float* ib) {
-  const DecodeParams& p = c.p;
+__device__ __noinline__ void task_dn_b(const DecodeParams& p, Ctl& C, uint32_t st, int part, float* ib,
+                                       uint64_t deadline) {
   const int lane = threadIdx.x & 31;
-  const int chunks = p.I / 8;
-  const int P = p.m * p.k;
-  const bool hs = p.sm_hs != 0;
-  const uint4* hbase;
-  if (hs) {
-    ensure_cache(c, CB_HS, &p.ctrl->shgu_done, (unsigned)c.z.n_shgu, p.shh, (uint32_t)(p.m * 2 * p.I), p.sm_hs);
-    hbase = reinterpret_cast<const uint4*>(smem_base() + p.sm_hs);
-  } else {
-    warp_wait(c, c.sh_ok, &p.ctrl->shgu_done, (unsigned)c.z.n_shgu);
-    hbase = reinterpret_cast<const uint4*>(p.shh);
-  }
-  const uint4* w = reinterpret_cast<const uint4*>(stage);
+  require(p, C, RQ_HS, deadline);
+#pragma unroll 1
   for (int t = 0; t < p.m; ++t) {
-    const uint4* hr = hbase + (size_t)t * chunks;
-    float2 acc[SDR];
-#pragma unroll
-    for (int r = 0; r < SDR; ++r) acc[r] = make_float2(0.f, 0.f);
-    for (int ch = lane; ch < chunks; ch += 32) {
-      const uint4 hv = hs ? hr[ch] : __ldcg(hr + ch);
-#pragma unroll
-      for (int r = 0; r < SDR; ++r) dot8(acc[r], w[r * chunks + ch], hv);
-    }
-#pragma unroll
-    for (int r = 0; r < SDR; ++r) {
-      const float s = warp_sum(acc[r].x + acc[r].y);
-      if (lane == 0) ib[(P + t) * DG + part * SDR + r] = s;
+    const float4 s = p.sm_hs ? bf16_rows_dot<2, true>(st, 2u * p.I, p.sm_hs + 2u * t * p.I, nullptr, p.I / 8)
+                             : bf16_rows_dot<2, false>(st, 2u * p.I, 0u, p.shh + (size_t)t * 2 * p.I, p.I / 8);
+    if (lane == 0) {
+      float* o = ib + (size_t)t * DG + part * SDR;
+      o[0] = s.x; o[1] = s.y;
     }
   }
 }
 
 // ------------------------------------------------------- item completion
-__device__ void complete_item(Ctx& c, const Item& it, float* ib) {
-  const DecodeParams& p = c.p;
+__device__ __noinline__ void complete_item(const DecodeParams& p, Ctl& C, Item it, float* ib, uint64_t deadline) {
   const int lane = threadIdx.x & 31;
   switch (it.kind) {
     case I_Q8:
@@ -556,40 +684,69 @@ __device__ void complete_item(Ctx& c, const Item& it, float* ib) {
       __threadfence();
       if (lane == 0) atomicAdd(&p.ctrl->router_done, 1u);
       break;
-    case I_SHGU_B:
+    case I_SHGU_B: {
+      // h = SwiGLU(g, u) of the item's rows, per token -> bf16
+      const int row0 = it.a * SHP, ns = min(SHP, p.I - row0);
+#pragma unroll 1
+      for (int q = lane; q < ns * p.m; q += 32) {
+        const int s = q / p.m, t = q % p.m;
+        const float g = ib[(size_t)(2 * s) * p.m + t], u = ib[(size_t)(2 * s + 1) * p.m + t];
+        reinterpret_cast<__nv_bfloat16*>(p.shh)[(size_t)t * p.I + row0 + s] =
+            __float2bfloat16_rn(swiglu_f32(g, u, p.swiglu_limit));
+      }
       __threadfence();
       if (lane == 0) atomicAdd(&p.ctrl->shgu_done, 1u);
       break;
+    }
     case I_GU: {
       // q8_1 of the item's 32 rows of h, per token
       const bool shared = it.a < 0;
       int ntok = p.m, vec0 = p.shvec0;
       bool present = true;
       if (!shared) {
-        const DecodePlan* plan = splan(c);
+        require(p, C, RQ_PLAN, deadline);
+        const DecodePlan* plan = plan_of(p);
         vec0 = plan->exp_off[it.a];
         ntok = plan->exp_off[it.a + 1] - vec0;
         present = plan->exp_ptr[it.a][0] != 0ull;
       }
+#pragma unroll 1
       for (int tt = 0; tt < ntok && present; ++tt)
         q8_block_warp(ib[lane * p.m + tt], it.b, nullptr, p.hu + (size_t)(vec0 + tt) * (unit_bytes(p.I) / 4));
       __threadfence();
       if (lane == 0) atomicAdd(shared ? &p.ctrl->shgu_done : &p.ctrl->rtgu_done, 1u);
       break;
     }
+    case I_SHDN: {
+      // y_shared of the group's rows -> out (the routed down item adds to it)
+#pragma unroll 1
+      for (int qd = lane; qd < p.m * DG; qd += 32) {
+        const int t = qd / DG, r = qd % DG;
+        p.out[(size_t)t * p.D + it.a * DG + r] = ib[t * DG + r];
+      }
+      __threadfence();
+      if (lane == 0) atomicAdd(&p.ctrl->shdn_done, 1u);
+      break;
+    }
     case I_DN: {
-      // y = sum over the token's pairs in ascending expert id of G E, then + S
-      const DecodePlan* plan = splan(c);
-      const int P = p.m * p.k;
+      // y = sum over the token's pairs in ascending expert id of G E, then
+      // + y_shared (every shared down item finished long before; the wait is
+      // bounded all the same)
+      require(p, C, RQ_PLAN, deadline);
+      if (lane == 0) wait_count(&p.ctrl->shdn_done, (unsigned)(p.D / DG), deadline, &p.ctrl->status);
+      __syncwarp();
+      const DecodePlan* plan = plan_of(p);
+#pragma unroll 1
       for (int qd = lane; qd < p.m * DG; qd += 32) {
         const int t = qd / DG, r = qd % DG;
         float acc = 0.f;
+#pragma unroll 1
         for (int i = 0; i < p.k; ++i) {
           const int pr = plan->tok_pairs[t][i];
           acc = fmaf(plan->pair_w[pr], ib[pr * DG + r], acc);
         }
-        acc += ib[(P + t) * DG + r];
-        p.out[(size_t)t * p.D + it.a * DG + r] = acc;
+        float* o = p.out + (size_t)t * p.D + it.a * DG + r;
+        *o = acc + __ldcg(o);
       }
       break;
     }
@@ -607,6 +764,7 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     for (int i = 0; i < NST; ++i) {
       mbar_init(bar(C.full[i]), 1);
       mbar_init(bar(C.empty[i]), 1);
+      C.hdr[i].seq = 0xFFFFFFFFu;
     }
     for (int i = 0; i < NIS; ++i) mbar_init(bar(C.item_done[i]), 1);
     mbar_init(bar(C.pbar), 1);
@@ -615,6 +773,9 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
       C.cstate[i] = 0u;
     }
     C.next = 0u;
+    C.rdy = 0u;
+    C.xq = 0u;
+    C.sink = 0u;
     fence_mbar_init();
   }
   __syncthreads();
@@ -626,12 +787,11 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     // Wait for every router row of the call, then build this block's plan.
     // On a timeout the plan is left empty (no routed expert work) so the
     // block still finishes; the status word already says why.
-    Ctx c{p, z, C, deadline, -1, false, false, false, false, false};
     bool ok = true;
     if (lane == 0) ok = wait_count(&p.ctrl->router_done, (unsigned)z.n_router, deadline, &p.ctrl->status);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) {
-      build_plan(c);
+      build_plan(p, C, deadline, p.sm_sel, p.sm_plan, false);
     } else if (lane == 0) {
       DecodePlan* plan = reinterpret_cast<DecodePlan*>(smem_base() + p.sm_plan);
       plan->n_exp = 0;
@@ -662,26 +822,61 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
       uint32_t j = 0;  // items started
       int n_exp = -1;
       bool ok = true;
+      bool local_done = false;
       const int rb = (p.D / QK) * Q2K_B, rb2 = (p.I / QK) * Q3K_B;
-      unsigned t_next = atomicAdd(&p.ctrl->ticket, 1u);
+      unsigned* const ctr[N_STREAMS] = {&p.ctrl->ticket, &p.ctrl->ticket_sh, &p.ctrl->ticket_gu, &p.ctrl->ticket_dn};
+      bool exhausted[N_STREAMS] = {false, false, false, false};
+      const DecodePlan* splan = reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan);
+      // the stream to take the next ticket from: -1 nothing left, N_STREAMS
+      // wait for the plan first
+      auto choose = [&]() -> int {
+        if (!exhausted[S_MAIN]) return S_MAIN;
+        if (n_exp < 0 && mbar_try_wait(bar(C.pbar), 0u)) n_exp = splan->n_exp;
+        if (n_exp >= 0 && !exhausted[S_GU]) return S_GU;
+        if (!exhausted[S_SHDN]) return S_SHDN;
+        if (n_exp < 0) return N_STREAMS;
+        return exhausted[S_DN] ? -1 : S_DN;
+      };
+      // one ticket is taken ahead, so that its atomic is in flight while
+      // the current item streams
+      int ps = -1;
+      unsigned pt = 0;
       for (;;) {
-        const unsigned t = t_next;
-        Item it = decode_ticket(t, z, groups, n_exp);
-        if (it.kind == -1) {
-          // the block's plan, built by the planner warp
-          if (!(ok = mbar_wait_bounded(bar(C.pbar), 0u, deadline, &p.ctrl->status))) break;
-          n_exp = reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan)->n_exp;
-          it = decode_ticket(t, z, groups, n_exp);
+        if (ps < 0) {
+          const int sel = choose();
+          if (sel < 0) break;
+          if (sel == N_STREAMS) {
+            if (!(ok = mbar_wait_bounded(bar(C.pbar), 0u, deadline, &p.ctrl->status))) break;
+            n_exp = splan->n_exp;
+            continue;
+          }
+          ps = sel;
+          pt = atomicAdd(ctr[sel], 1u);
         }
-        if (it.kind == -2) break;
-        t_next = atomicAdd(&p.ctrl->ticket, 1u);  // the next ticket is in flight while this item streams
+        Item it = decode_ticket(ps, pt, z, groups, n_exp);
+        if (it.kind == -2) {
+          exhausted[ps] = true;
+          ps = -1;
+          continue;
+        }
+        // the block-local item goes in before the block's first item past the router rows
+        if (!local_done && it.kind != I_Q8 && it.kind != I_ROUTER) {
+          local_done = true;
+          it = Item{I_LOCAL, 0, 0, 0, 0};  // the ticket stays taken for the next round
+        } else {
+          const int sel = choose();
+          ps = (sel >= 0 && sel < N_STREAMS) ? sel : -1;
+          if (ps >= 0) pt = atomicAdd(ctr[ps], 1u);
+        }
         int ns;
         switch (it.kind) {
           case I_Q8: ns = 1; break;
           case I_ROUTER: ns = 1; break;
-          case I_SHGU_B: ns = min(SHP, p.I - it.a * SHP); break;
+          case I_SHGU_B: ns = 2 * min(SHP, p.I - it.a * SHP); break;
           case I_GU: ns = GT / GR; break;
-          default: ns = z.dn_sh_parts + n_exp; break;
+          case I_SHDN: ns = z.dn_sh_parts; break;
+          case I_LOCAL: ns = NCW; break;
+          default: ns = n_exp; break;
         }
         const uint32_t islot = j % NIS;
         if (j >= (uint32_t)NIS &&
@@ -693,12 +888,15 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
           const uint32_t slot = n % NST, use = n / NST;
           if (use > 0 && !(ok = mbar_wait_bounded(bar(C.empty[slot]), (use - 1) & 1u, deadline, &p.ctrl->status)))
             break;
-          Hdr h{K_STOP, (int)islot, 0, 0};
+          Hdr h{K_STOP, (int)islot, 0, 0, n};
           const uint8_t *a = nullptr, *b = nullptr;
           uint32_t bytes = 0, boff = 0;
           switch (it.kind) {
             case I_Q8:
               h.kind = K_Q8; h.a = it.a;
+              break;
+            case I_LOCAL:
+              h.kind = K_LOCAL; h.a = s;
               break;
             case I_ROUTER: {
               const int r0 = it.a * RR;
@@ -708,12 +906,10 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
               break;
             }
             case I_SHGU_B: {
-              const int row = it.a * SHP + s;
-              h.kind = K_SHGU_B; h.a = row;
-              a = p.sh1 + (size_t)row * 2 * p.D;
-              b = p.sh3 + (size_t)row * 2 * p.D;
+              const int row = it.a * SHP + s / 2;
+              h.kind = K_SHGU_B; h.a = s / 2; h.b = s & 1;
+              a = ((s & 1) ? p.sh3 : p.sh1) + (size_t)row * 2 * p.D;
               bytes = (uint32_t)(2 * p.D);
-              boff = bytes;
               break;
             }
             case I_GU: {
@@ -735,20 +931,23 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
               }
               break;
             }
-            default: {  // I_DN: shared parts first, then the experts in ascending id
+            case I_SHDN: {  // the shared expert's rows of the group
               const int d0 = it.a * DG;
-              if (s < z.dn_sh_parts) {
-                if (z.shq) {
-                  h.kind = K_DN_SHQ;
-                  a = p.sh2 + (size_t)d0 * rb2;
-                  bytes = (uint32_t)(DG * rb2);
-                } else {
-                  h.kind = K_DN_SHB; h.a = s;
-                  a = p.sh2 + (size_t)(d0 + s * SDR) * 2 * p.I;
-                  bytes = (uint32_t)(SDR * 2 * p.I);
-                }
+              if (z.shq) {
+                h.kind = K_DN_SHQ;
+                a = p.sh2 + (size_t)d0 * rb2;
+                bytes = (uint32_t)(DG * rb2);
               } else {
-                const int e = s - z.dn_sh_parts;
+                h.kind = K_DN_SHB; h.a = s;
+                a = p.sh2 + (size_t)(d0 + s * SDR) * 2 * p.I;
+                bytes = (uint32_t)(SDR * 2 * p.I);
+              }
+              break;
+            }
+            default: {  // I_DN: the experts in ascending id
+              const int d0 = it.a * DG;
+              {
+                const int e = s;
                 h.kind = K_DN_RT; h.a = e;
                 const unsigned long long w2 =
                     reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan)->exp_ptr[e][2];
@@ -776,7 +975,7 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
           const uint32_t slot = n % NST, use = n / NST;
           if (use > 0 && !(ok = mbar_wait_bounded(bar(C.empty[slot]), (use - 1) & 1u, deadline, &p.ctrl->status)))
             break;
-          C.hdr[slot] = Hdr{K_STOP, 0, 0, 0};
+          C.hdr[slot] = Hdr{K_STOP, 0, 0, 0, n};
           mbar_arrive(bar(C.full[slot]));
           ++n;
         }
@@ -790,28 +989,44 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     }
   } else {
     // --------------------------------------------------------- consumers
-    Ctx c{p, z, C, deadline, -1, false, false, false, false, false};
     for (;;) {
       unsigned n = 0;
       if (lane == 0) n = atomicAdd(&C.next, 1u);
       n = __shfl_sync(0xffffffffu, n, 0);
       const uint32_t slot = n % NST;
+      // A consumer can be more than one ring turn ahead of the stage it took
+      // (copies land out of order), where the parity of the full barrier
+      // alone would also match the stage's previous use: wait first until the
+      // producer has written this stage's header, then for the barrier.
       bool got = true;
-      if (lane == 0) got = mbar_wait_bounded(bar(C.full[slot]), (n / NST) & 1u, deadline, &p.ctrl->status);
+      if (lane == 0) {
+        const volatile unsigned* seq = &C.hdr[slot].seq;
+        uint32_t spins = 0;
+        while (*seq != n) {
+          __nanosleep(32);
+          if ((++spins & 15u) == 0 && globaltimer_ns() > deadline) {
+            atomicOr(&p.ctrl->status, (unsigned)MOE_STATUS_TIMEOUT);
+            got = false;
+            break;
+          }
+        }
+        if (got) got = mbar_wait_bounded(bar(C.full[slot]), (n / NST) & 1u, deadline, &p.ctrl->status);
+      }
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       const Hdr h = C.hdr[slot];
       if (h.kind == K_STOP) break;
-      const uint8_t* st = smem_base() + (size_t)slot * SB;
+      const uint32_t st = slot * (uint32_t)SB;
       float* ib = item_buf(p, h.slot);
       switch (h.kind) {
-        case K_Q8: task_q8(c, h.a); break;
-        case K_ROUTER: task_router(c, st, h.a); break;
-        case K_SHGU_B: task_shgu_b(c, st, h.a); break;
-        case K_GU_Q: task_gu_q(c, st, h.a, h.b, ib); break;
-        case K_DN_SHB: task_dn_b(c, st, h.a, ib); break;
-        case K_DN_SHQ: task_dn_q(c, st, -1, ib); break;
-        case K_DN_RT: task_dn_q(c, st, h.a, ib); break;
+        case K_Q8: task_q8(p, h.a); break;
+        case K_ROUTER: task_router(p, C, st, h.a, deadline); break;
+        case K_SHGU_B: task_shgu_b(p, C, st, h.a, h.b, ib, deadline); break;
+        case K_LOCAL: task_local(p, C, st, h.a, deadline); break;
+        case K_GU_Q: task_gu_q(p, C, st, h.a, h.b, ib, deadline); break;
+        case K_DN_SHB: task_dn_b(p, C, st, h.a, ib, deadline); break;
+        case K_DN_SHQ:
+        case K_DN_RT: task_dn_q(p, C, st, h.kind == K_DN_RT ? h.a : -1, ib, deadline); break;
         default: break;
       }
       // release the stage, then count the task against its item
@@ -826,7 +1041,7 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
       if (left == 1u) {
         __threadfence_block();
         const Item it = C.item[h.slot];
-        complete_item(c, it, ib);
+        complete_item(p, C, it, ib, deadline);
         __syncwarp();
         __threadfence_block();
         if (lane == 0) mbar_arrive(bar(C.item_done[h.slot]));
@@ -840,10 +1055,14 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     const unsigned old = atomicAdd(&p.ctrl->exit_count, 1u);
     if (old == gridDim.x - 1) {
       p.ctrl->ticket = 0u;
+      p.ctrl->ticket_sh = 0u;
+      p.ctrl->ticket_gu = 0u;
+      p.ctrl->ticket_dn = 0u;
       p.ctrl->q8_done = 0u;
       p.ctrl->router_done = 0u;
       p.ctrl->shgu_done = 0u;
       p.ctrl->rtgu_done = 0u;
+      p.ctrl->shdn_done = 0u;
       __threadfence();
       p.ctrl->exit_count = 0u;
     }
@@ -862,8 +1081,8 @@ bool plan_smem(DecodeParams& p) {
   p.sm_plan = (uint32_t)off;
   off = a16(off + sizeof(DecodePlan));
   const size_t P = (size_t)p.m * p.k;
-  const size_t gu = (size_t)GT * p.m * 4, dn = (P + p.m) * DG * 4;
-  p.item_bytes = (uint32_t)a16(gu > dn ? gu : dn);
+  const size_t gu = (size_t)GT * p.m * 4, dn = (P + p.m) * DG * 4, sg = (size_t)2 * SHP * p.m * 4;
+  p.item_bytes = (uint32_t)a16(std::max(std::max(gu, dn), sg));
   p.sm_items = (uint32_t)off;
   off += (size_t)NIS * p.item_bytes;
   p.sm_sel = (uint32_t)off;
@@ -892,7 +1111,7 @@ bool plan_smem(DecodeParams& p) {
 
 bool decode_fits(int D, int I) {
   const int rb = (D / QK) * Q2K_B, rb2 = (I / QK) * Q3K_B;
-  return 2 * GR * rb <= SB && DG * rb2 <= SB && RR * 2 * D <= SB && 4 * D <= SB && SDR * 2 * I <= SB &&
+  return 2 * GR * rb <= SB && DG * rb2 <= SB && RR * 2 * D <= SB && 2 * D <= SB && SDR * 2 * I <= SB &&
          D % DG == 0 && I % GT == 0;
 }
 

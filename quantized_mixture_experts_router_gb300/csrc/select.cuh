@@ -52,6 +52,28 @@ static __device__ __forceinline__ float score_fast(float z, float T) {
   return __fsqrt_rn(log1pf(expf(t)));
 }
 
+// Routing weights from the picks: lane r < k holds pick r (id, score).  The
+// sum runs in pick order (every lane computes it), then lane r writes weight
+// r: score / (sum + 1e-20) when norm and k > 1, times route_scale.
+static __device__ __forceinline__ void write_picks(int my_id, float my_s, int k, int norm, float route_scale,
+                                                   float* w_out, int* idx_out, int* pick_id, float* pick_w) {
+  const int lane = threadIdx.x & 31;
+  float sum = 0.f;
+#pragma unroll 1
+  for (int q = 0; q < k; ++q) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_s, q));
+  sum = __fadd_rn(sum, 1e-20f);
+  if (lane < k) {
+    const float wv = __fmul_rn(norm && k > 1 ? __fdiv_rn(my_s, sum) : my_s, route_scale);
+    w_out[lane] = wv;
+    idx_out[lane] = my_id;
+    if (pick_id) {
+      pick_id[lane] = my_id;
+      pick_w[lane] = wv;
+    }
+  }
+  __syncwarp();
+}
+
 // Scratch one warp needs in shared memory for one token: 3 * N words.
 __host__ __device__ inline size_t select_scratch_bytes(int N) { return (size_t)3 * N * 4; }
 
@@ -115,9 +137,10 @@ static __device__ __noinline__ void route_token_warp(const float* __restrict__ z
   uint32_t taken = 0;
   float prev_key = 0.f, kth_key = 0.f;
   bool resolved = true;
-  int picked_id[MAX_TOPK];
-  float picked_s[MAX_TOPK];
+  int my_id = 0;  // lane r < k: pick r
+  float my_s = 0.f;
   const int rounds = k < N ? k + 1 : k;
+#pragma unroll 1
   for (int r = 0; r < rounds; ++r) {
     unsigned long long best = 0;
     for (int e = lane, i = 0; e < N; e += 32, ++i) {
@@ -134,8 +157,10 @@ static __device__ __noinline__ void route_token_warp(const float* __restrict__ z
     if (r > 0 && !(prev_key - wk > 2.0f * eps)) resolved = false;
     prev_key = wk;
     if (r < k) {
-      picked_id[r] = win;
-      picked_s[r] = ssc[win];
+      if (lane == r) {
+        my_id = win;
+        my_s = ssc[win];
+      }
       kth_key = wk;
     }
   }
@@ -161,6 +186,7 @@ static __device__ __noinline__ void route_token_warp(const float* __restrict__ z
     }
     __syncwarp();
     uint32_t used = 0;  // bit c of lane's mask: candidate lane + 32 c taken
+#pragma unroll 1
     for (int r = 0; r < k; ++r) {
       unsigned long long best = 0;
       for (int c = lane, i = 0; c < nc; c += 32, ++i) {
@@ -173,32 +199,16 @@ static __device__ __noinline__ void route_token_warp(const float* __restrict__ z
       }
       const unsigned long long wmax = warp_max_u64(best);
       const int win = (int)(0xFFFFFFFFu - (uint32_t)(wmax & 0xFFFFFFFFu));
-      picked_id[r] = win;
-      picked_s[r] = ssc[win];
+      if (lane == r) {
+        my_id = win;
+        my_s = ssc[win];
+      }
       for (int c = lane, i = 0; c < nc; c += 32, ++i)
         if (slist[c] == win) used |= 1u << i;
     }
   }
-  if (lane == 0) {
-    float w[MAX_TOPK];
-    for (int r = 0; r < k; ++r) w[r] = picked_s[r];
-    if (norm && k > 1) {
-      float sum = 0.f;
-      for (int r = 0; r < k; ++r) sum = __fadd_rn(sum, w[r]);
-      sum = __fadd_rn(sum, 1e-20f);
-      for (int r = 0; r < k; ++r) w[r] = __fdiv_rn(w[r], sum);
-    }
-    for (int r = 0; r < k; ++r) {
-      const float wr = __fmul_rn(w[r], route_scale);
-      w_out[r] = wr;
-      idx_out[r] = picked_id[r];
-      if (pick_id) {
-        pick_id[r] = picked_id[r];
-        pick_w[r] = wr;
-      }
-    }
-  }
   __syncwarp();
+  write_picks(my_id, my_s, k, norm, route_scale, w_out, idx_out, pick_id, pick_w);
 }
 
 // The same routing with up to 12 keys per lane held in registers (N <= 384),
@@ -243,11 +253,10 @@ static __device__ __noinline__ void route_token_warp_r12(const float* __restrict
   uint32_t taken = 0;
   float prev_key = 0.f;
   bool resolved = true;
-  int pid[MAX_TOPK];
-  float ps[MAX_TOPK];
-#pragma unroll
-  for (int q = 0; q < MAX_TOPK; ++q) { pid[q] = 0; ps[q] = 0.f; }
+  int my_id = 0;  // lane r < k: pick r
+  float my_s = 0.f;
   const int rounds = k < N ? k + 1 : k;
+#pragma unroll 1
   for (int r = 0; r < rounds; ++r) {
     unsigned long long best = 0;
     float bk = 0.f, bs = 0.f;
@@ -266,33 +275,16 @@ static __device__ __noinline__ void route_token_warp_r12(const float* __restrict
     if ((win & 31) == lane) taken |= 1u << (win >> 5);
     if (r > 0 && !(prev_key - wk > 2.0f * eps)) resolved = false;
     prev_key = wk;
-#pragma unroll
-    for (int q = 0; q < MAX_TOPK; ++q)
-      if (q == r) { pid[q] = win; ps[q] = ws; }
+    if (r < k && lane == r) {
+      my_id = win;
+      my_s = ws;
+    }
   }
   if (!resolved) {
     route_token_warp(z, sk, bias, N, k, T, norm, route_scale, w_out, idx_out, status, scratch, pick_id, pick_w);
     return;
   }
-  if (lane == 0) {
-    float sum = 0.f;
-#pragma unroll
-    for (int q = 0; q < MAX_TOPK; ++q)
-      if (q < k) sum = __fadd_rn(sum, ps[q]);
-    sum = __fadd_rn(sum, 1e-20f);
-    const bool nrm = norm && k > 1;
-#pragma unroll
-    for (int q = 0; q < MAX_TOPK; ++q) {
-      if (q < k) {
-        const float wv = __fmul_rn(nrm ? __fdiv_rn(ps[q], sum) : ps[q], route_scale);
-        w_out[q] = wv;
-        idx_out[q] = pid[q];
-        pick_id[q] = pid[q];
-        pick_w[q] = wv;
-      }
-    }
-  }
-  __syncwarp();
+  write_picks(my_id, my_s, k, norm, route_scale, w_out, idx_out, pick_id, pick_w);
 }
 
 }  // namespace moe
