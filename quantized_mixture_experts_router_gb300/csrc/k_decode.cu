@@ -29,9 +29,7 @@
 // of one SM run different task kinds at once; a miss costs a trip to L2,
 // which under the full streaming load takes microseconds.  So every task kind
 // is one out-of-line routine with rolled loops, called from a single site,
-// the readiness of inputs is a block-level bit in shared memory, and every
-// block runs its routines once on scratch bytes right after its router rows
-// (the block-local item) so that they are cached before their phase.
+// and the readiness of inputs is a block-level bit in shared memory.
 //
 // Method: DeepSeek V4.1 atlas "Mixture of experts" (Router, Routed expert and
 // Shared expert steps: g' = min(g, L), u' = clip(u, -L, L), h = g' sigmoid(g') u',
@@ -97,7 +95,6 @@ struct Ctl {
   unsigned next;                  // consumer grab counter
   unsigned rdy;                   // RQ_* bits: inputs ready for every warp of the block
   unsigned xq;                    // consumer warps done with their share of q8_1(x)
-  unsigned sink;                  // written only if a scratch pass returns an impossible value
 };
 
 __device__ __forceinline__ uint8_t* smem_base() {
@@ -376,13 +373,6 @@ __device__ __noinline__ void require(const DecodeParams& p, Ctl& C, unsigned bit
   __syncwarp();
 }
 
-__host__ __device__ __forceinline__ size_t a16d(size_t v) { return (v + 15) & ~size_t(15); }
-
-// the selection scratch, picks and sorted pairs, then the plan
-__host__ __device__ __forceinline__ size_t plan_scratch_bytes(int N) {
-  return a16d(select_scratch_bytes(N) + (size_t)4 * MAXP * 4) + sizeof(DecodePlan);
-}
-
 __device__ __forceinline__ const DecodePlan* plan_of(const DecodeParams& p) {
   return reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan);
 }
@@ -394,19 +384,16 @@ __device__ __forceinline__ const DecodePlan* plan_of(const DecodeParams& p) {
 // computes the same plan; block 0 also writes the routing outputs).  Under
 // full load every dependent global round trip costs microseconds, so the
 // plan never goes through global memory.
-// sel, plan: shared-memory offsets of the selection scratch and of the plan.
-// dry: a run on scratch space only (the block-local item's cache warm-up),
-// which writes nothing outside shared memory and leaves the status alone.
-__device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t deadline, uint32_t sel,
-                                        uint32_t plan_off, bool dry) {
+__device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t deadline) {
+  const uint32_t sel = p.sm_sel, plan_off = p.sm_plan;
   const int lane = threadIdx.x & 31;
   float* scratch = reinterpret_cast<float*>(smem_base() + sel);
   int* pk_id = reinterpret_cast<int*>(smem_base() + sel + select_scratch_bytes(p.N));
   float* pk_w = reinterpret_cast<float*>(pk_id + MAXP);
   int* s_e = pk_id + 2 * MAXP;  // expert of each sorted position
   int* s_t = pk_id + 3 * MAXP;  // token of each sorted position
-  const bool writer = blockIdx.x == 0 && !dry;
-  unsigned* status = dry ? &C.sink : &p.ctrl->status;
+  const bool writer = blockIdx.x == 0;
+  unsigned* status = &p.ctrl->status;
 #pragma unroll 1
   for (int t = 0; t < p.m; ++t) {
     float* wo = writer ? p.topk_w + (size_t)t * p.k : pk_w + t * p.k;
@@ -509,15 +496,9 @@ __device__ __noinline__ void quantize_x_smem(const DecodeParams& p, int first, i
 }
 
 // Block-local work, NCW tasks per block issued after the block's router rows:
-// share `part` of q8_1(x) into shared memory, and one pass of a row routine
-// on scratch bytes of the ring (results discarded) so that the routines the
-// later phases run are already in the instruction cache.
-__device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t deadline, uint32_t sel,
-                                        uint32_t plan_off, bool dry);
-
-// (Part NCW/2 instead runs the selection and the plan builder dry, on its own
-// stage as scratch, for the planner warp that runs them for real later.)
-__device__ __noinline__ void task_local(const DecodeParams& p, Ctl& C, uint32_t st, int part, uint64_t deadline) {
+// share `part` of q8_1(x) into shared memory.  Eight warps run the code at
+// once, so its instruction-cache misses are paid once per SM, not per warp.
+__device__ __noinline__ void task_local(const DecodeParams& p, Ctl& C, int part, uint64_t deadline) {
   const int lane = threadIdx.x & 31;
   if (p.sm_x) {
     require(p, C, RQ_XB, deadline);
@@ -526,21 +507,6 @@ __device__ __noinline__ void task_local(const DecodeParams& p, Ctl& C, uint32_t 
     __threadfence_block();
     if (lane == 0) atomicAdd(&C.xq, 1u);
   }
-  if (part == NCW / 2 && plan_scratch_bytes(p.N) <= (size_t)SB) {
-    build_plan(p, C, deadline, st, st + (uint32_t)a16d(select_scratch_bytes(p.N) + (size_t)4 * MAXP * 4), true);
-    return;
-  }
-  float sink = 0.f;
-  const uint32_t sv = (uint32_t)SB;  // scratch bytes of stage 1
-  switch (part & 3) {
-    case 0: sink = bf16_rows_dot<1, true>(0u, 0u, sv, nullptr, min(p.D / 8, 256)).x; break;
-    case 1: sink = bf16_rows_dot<2, true>(0u, 2u * p.I, sv, nullptr, min(p.I / 8, 256)).x; break;
-    case 2: sink = q2k_rows4_dot<true>(0u, (p.D / QK) * Q2K_B, min(p.D / 64, 64), sv, nullptr).x; break;
-    default:
-      sink = q3k_row_dot<true>((uint32_t)((lane >> 2) * (p.I / QK) * Q3K_B), min(p.I / 64, 64), sv, nullptr);
-      break;
-  }
-  if (sink == 1.2345678e-30f) C.sink = 1u;
 }
 
 // router row e (stage offset st) against every token -> the logit and the
@@ -775,7 +741,6 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     C.next = 0u;
     C.rdy = 0u;
     C.xq = 0u;
-    C.sink = 0u;
     fence_mbar_init();
   }
   __syncthreads();
@@ -791,7 +756,7 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     if (lane == 0) ok = wait_count(&p.ctrl->router_done, (unsigned)z.n_router, deadline, &p.ctrl->status);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) {
-      build_plan(p, C, deadline, p.sm_sel, p.sm_plan, false);
+      build_plan(p, C, deadline);
     } else if (lane == 0) {
       DecodePlan* plan = reinterpret_cast<DecodePlan*>(smem_base() + p.sm_plan);
       plan->n_exp = 0;
@@ -1022,7 +987,7 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
         case K_Q8: task_q8(p, h.a); break;
         case K_ROUTER: task_router(p, C, st, h.a, deadline); break;
         case K_SHGU_B: task_shgu_b(p, C, st, h.a, h.b, ib, deadline); break;
-        case K_LOCAL: task_local(p, C, st, h.a, deadline); break;
+        case K_LOCAL: task_local(p, C, h.a, deadline); break;
         case K_GU_Q: task_gu_q(p, C, st, h.a, h.b, ib, deadline); break;
         case K_DN_SHB: task_dn_b(p, C, st, h.a, ib, deadline); break;
         case K_DN_SHQ:

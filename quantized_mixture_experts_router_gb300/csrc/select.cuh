@@ -256,20 +256,28 @@ static __device__ __noinline__ void route_token_warp_r12(const float* __restrict
   int my_id = 0;  // lane r < k: pick r
   float my_s = 0.f;
   const int rounds = k < N ? k + 1 : k;
+  // order-preserving key bits (the high word of rank_key), computed once
+  uint32_t ku[PL];
+#pragma unroll
+  for (int i = 0; i < PL; ++i) ku[i] = (uint32_t)(rank_key(kf[i], 0) >> 32);
 #pragma unroll 1
   for (int r = 0; r < rounds; ++r) {
-    unsigned long long best = 0;
+    // the lane's best untaken key (ties: the lower index, i.e. the lower id)
+    uint32_t best = 0;
+    int bi = -1;
     float bk = 0.f, bs = 0.f;
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < N && !(taken >> i & 1u)) {
-        const unsigned long long rk = rank_key(kf[i], e);
-        if (rk > best) { best = rk; bk = kf[i]; bs = sf[i]; }
+      if (lane + 32 * i < N && !(taken >> i & 1u) && (bi < 0 || ku[i] > best)) {
+        best = ku[i]; bi = i; bk = kf[i]; bs = sf[i];
       }
     }
-    const unsigned long long wmax = warp_max_u64(best);
-    const int win = (int)(0xFFFFFFFFu - (uint32_t)(wmax & 0xFFFFFFFFu));
+    // the warp's largest key, then the lowest id among the lanes holding it
+    // (a lane with nothing left offers no id; NaN keys, bits 0, still win
+    // over nothing)
+    const uint32_t top = __reduce_max_sync(0xffffffffu, best);
+    const uint32_t cand = (bi >= 0 && best == top) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
+    const int win = (int)__reduce_min_sync(0xffffffffu, cand);
     const float wk = __shfl_sync(0xffffffffu, bk, win & 31);
     const float ws = __shfl_sync(0xffffffffu, bs, win & 31);
     if ((win & 31) == lane) taken |= 1u << (win >> 5);
