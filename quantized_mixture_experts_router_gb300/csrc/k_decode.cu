@@ -185,12 +185,24 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// c + a*b for the low (hi = 0) or high bf16 halves of a and b, with one f32
+// rounding: the mixed-precision fma takes the bf16 operands directly, the same
+// result as fmaf on the widened values without the two unpacking instructions.
+__device__ __forceinline__ float fma_bf16(uint32_t a, uint32_t b, float c, int hi) {
+  unsigned short al, ah, bl, bh;
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(al), "=h"(ah) : "r"(a));
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(bl), "=h"(bh) : "r"(b));
+  if (hi) asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(c) : "h"(ah), "h"(bh));
+  else asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(c) : "h"(al), "h"(bl));
+  return c;
+}
+
 // 8 bf16 products into two accumulators (two independent FMA chains)
 __device__ __forceinline__ void dot8(float2& acc, const uint4& w, const uint4& x) {
-  acc.x = fmaf(bf16lo(w.x), bf16lo(x.x), acc.x); acc.y = fmaf(bf16hi(w.x), bf16hi(x.x), acc.y);
-  acc.x = fmaf(bf16lo(w.y), bf16lo(x.y), acc.x); acc.y = fmaf(bf16hi(w.y), bf16hi(x.y), acc.y);
-  acc.x = fmaf(bf16lo(w.z), bf16lo(x.z), acc.x); acc.y = fmaf(bf16hi(w.z), bf16hi(x.z), acc.y);
-  acc.x = fmaf(bf16lo(w.w), bf16lo(x.w), acc.x); acc.y = fmaf(bf16hi(w.w), bf16hi(x.w), acc.y);
+  acc.x = fma_bf16(w.x, x.x, acc.x, 0); acc.y = fma_bf16(w.x, x.x, acc.y, 1);
+  acc.x = fma_bf16(w.y, x.y, acc.x, 0); acc.y = fma_bf16(w.y, x.y, acc.y, 1);
+  acc.x = fma_bf16(w.z, x.z, acc.x, 0); acc.y = fma_bf16(w.z, x.z, acc.y, 1);
+  acc.x = fma_bf16(w.w, x.w, acc.x, 0); acc.y = fma_bf16(w.w, x.w, acc.y, 1);
 }
 
 // 16 bytes of an activation vector: from the block's shared-memory copy (S,
