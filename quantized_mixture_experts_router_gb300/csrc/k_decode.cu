@@ -806,11 +806,19 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
       const DecodePlan* splan = reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan);
       // the stream to take the next ticket from: -1 nothing left, N_STREAMS
       // wait for the plan first
+      // Before the plan exists, shared down items are taken only once the
+      // shared h is complete: their tasks would otherwise hold ring stages
+      // while they wait, and the routed gate/up items could not get in.
+      bool sh_ready = false;
+      auto shared_ready = [&]() -> bool {
+        if (!sh_ready) sh_ready = ld_acquire(&p.ctrl->shgu_done) >= (unsigned)z.n_shgu;
+        return sh_ready;
+      };
       auto choose = [&]() -> int {
         if (!exhausted[S_MAIN]) return S_MAIN;
         if (n_exp < 0 && mbar_try_wait(bar(C.pbar), 0u)) n_exp = splan->n_exp;
         if (n_exp >= 0 && !exhausted[S_GU]) return S_GU;
-        if (!exhausted[S_SHDN]) return S_SHDN;
+        if (!exhausted[S_SHDN] && (n_exp >= 0 || shared_ready())) return S_SHDN;
         if (n_exp < 0) return N_STREAMS;
         return exhausted[S_DN] ? -1 : S_DN;
       };
@@ -823,8 +831,22 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
           const int sel = choose();
           if (sel < 0) break;
           if (sel == N_STREAMS) {
-            if (!(ok = mbar_wait_bounded(bar(C.pbar), 0u, deadline, &p.ctrl->status))) break;
-            n_exp = splan->n_exp;
+            // wait for the plan, or for the shared h while shared down items are left
+            uint32_t spins = 0;
+            for (;;) {
+              if (mbar_try_wait(bar(C.pbar), 0u)) {
+                n_exp = splan->n_exp;
+                break;
+              }
+              if (!exhausted[S_SHDN] && shared_ready()) break;
+              __nanosleep(200);
+              if ((++spins & 15u) == 0 && globaltimer_ns() > deadline) {
+                atomicOr(&p.ctrl->status, (unsigned)MOE_STATUS_TIMEOUT);
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
             continue;
           }
           ps = sel;
