@@ -71,7 +71,7 @@ enum : int { I_Q8 = 0, I_ROUTER, I_SHGU_B, I_GU, I_SHDN, I_DN, I_LOCAL };
 // shared-memory copies: x (bf16), routed h units, shared h, q8_1(x) units, expert pointer table, bias
 enum : int { CB_XB = 0, CB_HR, CB_HS, CB_XU, CB_EP, CB_BIAS, N_CB };
 // block-level readiness of the inputs a task reads (bits of Ctl::rdy)
-enum : unsigned { RQ_XB = 1u, RQ_BIAS = 2u, RQ_XU = 4u, RQ_HR = 8u, RQ_HS = 16u, RQ_PLAN = 32u };
+enum : unsigned { RQ_XB = 1u, RQ_BIAS = 2u, RQ_XU = 4u, RQ_HR = 8u, RQ_HS = 16u, RQ_PLAN = 32u, RQ_SHDN = 64u };
 
 struct Hdr {
   int kind, slot, a, b;
@@ -374,6 +374,9 @@ __device__ __noinline__ void require(const DecodeParams& p, Ctl& C, unsigned bit
           else
             fill_or_wait(C, CB_HS, &p.ctrl->shgu_done, (unsigned)z.n_shgu, p.shh, (uint32_t)(p.m * 2 * p.I),
                          p.sm_hs, deadline, st);
+          break;
+        case RQ_SHDN:
+          wait_count(&p.ctrl->shdn_done, (unsigned)(p.D / DG), deadline, st);
           break;
         default:
           break;
@@ -710,9 +713,7 @@ __device__ __noinline__ void complete_item(const DecodeParams& p, Ctl& C, Item i
       // y = sum over the token's pairs in ascending expert id of G E, then
       // + y_shared (every shared down item finished long before; the wait is
       // bounded all the same)
-      require(p, C, RQ_PLAN, deadline);
-      if (lane == 0) wait_count(&p.ctrl->shdn_done, (unsigned)(p.D / DG), deadline, &p.ctrl->status);
-      __syncwarp();
+      require(p, C, RQ_PLAN | RQ_SHDN, deadline);
       const DecodePlan* plan = plan_of(p);
 #pragma unroll 1
       for (int qd = lane; qd < p.m * DG; qd += 32) {
