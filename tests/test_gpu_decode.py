@@ -3,6 +3,8 @@
 Bars: q8_1(x) bit-exact; top-k indices bit-exact on identical f32 logits
 (both directions); outputs and routing weights within 2e-3 relative L2 and
 max-abs <= 1e-2 x RMS of the oracle output."""
+import time
+
 import numpy as np
 import pytest
 
@@ -193,6 +195,32 @@ def test_missing_expert_status():
     keep = [t for t in range(w.m) if victim not in first["topk_idx"][t]]
     if keep:
         np.testing.assert_allclose(res["out"][keep], first["out"][keep], rtol=1e-6, atol=1e-6)
+
+
+def test_wait_timeout_sets_status_and_returns():
+    """Every in-kernel wait is bounded.  A ticket counter pushed past every
+    item leaves the router count unreachable: the planner, the producer and
+    the consumers give up after wait_timeout_us, the call ends with
+    MOE_STATUS_TIMEOUT, and the next call on the re-initialised workspace is
+    correct (the context stays usable; no fault, no trap)."""
+    w = W.WORKLOADS["tiny"].with_(m=2)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    cfg = lib_cfg(w, path=Q.MOE_PATH_DECODE, timeout_us=20000)
+    ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    Q.moe_v41_workspace_init(ws)
+    # control block: status, route_arrive, then the decode ticket counter (u32 at byte 8)
+    ws[8:12].view(torch.int32).fill_(0x40000000)
+    t0 = time.perf_counter()
+    res = gpu_forward(dl, path=Q.MOE_PATH_DECODE, ws=ws, cfg=cfg)
+    elapsed = time.perf_counter() - t0
+    assert res["status"] & Q.MOE_STATUS_TIMEOUT
+    assert elapsed < 5.0
+    Q.moe_v41_workspace_init(ws)
+    good = gpu_forward(dl, path=Q.MOE_PATH_DECODE, ws=ws, cfg=cfg)
+    assert good["status"] == 0
+    r = oracle_for(w, 0, given_logits=good["logits"])
+    np.testing.assert_array_equal(good["topk_idx"], r.topk_idx)
+    assert_close(good["out"], r.out, "output after a timed-out call")
 
 
 def test_argument_errors():
