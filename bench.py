@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=30)
     ap.add_argument("--prefill-m", type=int, default=0, help="tokens of the prefill call (default: the workload's)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--graph", type=int, default=1,
+                    help="1: time the decode step as one CUDA-graph replay of its layer calls; 0: eager launches")
     return ap.parse_args()
 
 
@@ -278,9 +280,10 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def layer_call(l, x=None):
+        # on the current stream: the launch stream, or the capture stream of a graph
         d = layers[l % resident]
         Q.moe_v41_forward(cfg, xs[l] if x is None else x, w.m, d.router_w, d.bias, d.expert_ptrs, w.shared_kind,
-                          d.sh1, d.sh3, d.sh2, out[l], tw[l], ti[l], None, ws, stream)
+                          d.sh1, d.sh3, d.sh2, out[l], tw[l], ti[l], None, ws)
 
     def barrier():
         if world > 1:
@@ -296,9 +299,20 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {st} during warm-up")
     distinct = float(np.mean([np.unique(ti[l].cpu().numpy()).size for l in range(L)]))
 
-    # --- device-resident timed region, one event per layer boundary
+    # --- device-resident timed region: the step's L layer calls captured once
+    # as a CUDA graph and replayed K times (routing never leaves the device,
+    # so a step has no host round trip), or launched eagerly with one event
+    # per layer boundary
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(K)]
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for l in range(L):
+                layer_call(l)
+        graph.replay()
+        torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(K)] if graph is None else []
     barrier()
     clocks = Clocks(local_rank)
     clocks.start()
@@ -306,6 +320,9 @@ def run_ours(args, rank, world, local_rank):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(K):
+        if graph is not None:
+            graph.replay()
+            continue
         for l in range(L):
             evs[k][l].record(stream)
             layer_call(l)
@@ -314,7 +331,10 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end)
-    per_call_ms = statistics.fmean(evs[k][l].elapsed_time(evs[k][l + 1]) for k in range(K) for l in range(L))
+    if graph is not None:
+        per_call_ms = ms / (K * L)
+    else:
+        per_call_ms = statistics.fmean(evs[k][l].elapsed_time(evs[k][l + 1]) for k in range(K) for l in range(L))
     st = Q.moe_v41_read_status(ws, stream, clear=True)
     if st:
         raise RuntimeError(f"device status {st} during the timed region")
@@ -356,10 +376,10 @@ def run_ours(args, rank, world, local_rank):
         if e2e:
             e2e["ms"] = float(t[1])
     launches = Q.moe_v41_kernel_launches(cfg, w.m, w.shared_kind)
-    del layers, xs, out, tw, ti, ws
+    del graph, layers, xs, out, tw, ti, ws
     torch.cuda.empty_cache()
     return dict(w=w, L=L, K=K, ms=ms, per_call_ms=per_call_ms, distinct=distinct, clocks=clk, e2e=e2e,
-                resident=resident, rotated=rotated, launches_per_call=launches,
+                resident=resident, rotated=rotated, launches_per_call=launches, graph=bool(args.graph),
                 kernel=("k_decode_layer (the whole layer call, one launch)" if launches == 1 else
                         f"the prefill kernels of one layer call ({launches} launches)"),
                 resident_experts=args.resident_experts)
@@ -542,6 +562,9 @@ def config_of(w: W.Workload, L: int, r):
     if r:
         c["distinct_experts_per_call"] = r["distinct"]
         c["resident_layers"] = r["resident"]
+        if "graph" in r:
+            c["launch"] = ("the step's layer calls captured once as a CUDA graph, replayed per step"
+                           if r["graph"] else "eager launches, one event per layer boundary")
         if r.get("resident_experts"):
             c["resident_experts"] = r["resident_experts"]
             c["note_experts"] = "profiling run: expert e uses slot e % resident_experts"

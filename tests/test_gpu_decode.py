@@ -223,6 +223,40 @@ def test_wait_timeout_sets_status_and_returns():
     assert_close(good["out"], r.out, "output after a timed-out call")
 
 
+def test_graph_replay_matches_eager():
+    """A decode step (three layer calls) captured as a CUDA graph and replayed
+    gives the eager launches' results bit for bit: the call has no host round
+    trip, and the kernel resets its call-wide counters itself."""
+    w = W.WORKLOADS["tiny"].with_(m=3)
+    layers = [stage_layer(w, l, experts_on_gpu=False) for l in range(3)]
+    cfg = lib_cfg(w, path=Q.MOE_PATH_DECODE)
+    ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    Q.moe_v41_workspace_init(ws)
+    outs = [torch.empty((w.m, w.dim), device="cuda") for _ in layers]
+    tws = [torch.empty((w.m, w.topk), device="cuda") for _ in layers]
+    tis = [torch.empty((w.m, w.topk), dtype=torch.int32, device="cuda") for _ in layers]
+
+    def step():
+        for l, d in enumerate(layers):
+            Q.moe_v41_forward(cfg, d.x, w.m, d.router_w, d.bias, d.expert_ptrs, w.shared_kind, d.sh1, d.sh3, d.sh2,
+                              outs[l], tws[l], tis[l], None, ws)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [(o.clone(), t.clone(), i.clone()) for o, t, i in zip(outs, tws, tis)]
+    for o in outs:
+        o.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert Q.moe_v41_read_status(ws, clear=True) == 0
+    for (eo, et, ei), o, t, i in zip(eager, outs, tws, tis):
+        assert torch.equal(eo, o) and torch.equal(et, t) and torch.equal(ei, i)
+
+
 def test_argument_errors():
     w = W.WORKLOADS["tiny"]
     cfg = lib_cfg(w)
