@@ -342,26 +342,39 @@ def run_ours(args, rank, world, local_rank):
     # --- end to end through host buffers
     e2e = None
     if not args.no_e2e:
-        xh = [torch.empty((w.m, w.dim), dtype=torch.int16).pin_memory() for _ in range(L)]
+        # the step's inputs and results as one pinned buffer each: one host->device
+        # copy in and one device->host copy out per step
+        xh = torch.empty((L, w.m, w.dim), dtype=torch.int16).pin_memory()
         for l in range(L):
             xh[l].copy_(xs[l].cpu())
         oh = torch.empty((L, w.m, w.dim), dtype=torch.float32).pin_memory()
         xd = torch.empty((L, w.m, w.dim), dtype=torch.int16, device=dev)
         Ke = max(1, K // 2)
-        for _ in range(2):
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
             for l in range(L):
-                xd[l].copy_(xh[l], non_blocking=True)
                 layer_call(l, xd[l])
-                oh[l].copy_(out[l], non_blocking=True)
+            oh.copy_(out, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
         barrier()
+        # the same capture as the device-resident region, host copies included
+        e2e_graph = None
+        if args.graph:
+            e2e_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(e2e_graph):
+                e2e_step()
+            e2e_graph.replay()
+            barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(Ke):
-            for l in range(L):
-                xd[l].copy_(xh[l], non_blocking=True)
-                layer_call(l, xd[l])
-                oh[l].copy_(out[l], non_blocking=True)
+            if e2e_graph is not None:
+                e2e_graph.replay()
+            else:
+                e2e_step()
         e1.record(stream)
         barrier()
         e_ms = e0.elapsed_time(e1)
