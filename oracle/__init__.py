@@ -23,13 +23,17 @@ SHARED_KQUANT = 1
 class Cfg(ctypes.Structure):
     _fields_ = [("dim", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_routed", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("gate_temp", ctypes.c_float), ("norm_topk_prob", ctypes.c_int32),
-                ("route_scale", ctypes.c_float), ("swiglu_limit", ctypes.c_float)]
+                ("route_scale", ctypes.c_float), ("swiglu_limit", ctypes.c_float), ("score_func", ctypes.c_int32)]
+
+
+SCORE_SQRTSOFTPLUS, SCORE_SIGMOID, SCORE_SOFTMAX = 0, 1, 2
 
 
 class Layer(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("router_w", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("given_logits", ctypes.c_void_p), ("experts", ctypes.c_void_p), ("shared_kind", ctypes.c_int32),
-                ("sh1", ctypes.c_void_p), ("sh3", ctypes.c_void_p), ("sh2", ctypes.c_void_p)]
+                ("sh1", ctypes.c_void_p), ("sh3", ctypes.c_void_p), ("sh2", ctypes.c_void_p),
+                ("bias_vl", ctypes.c_void_p), ("image_mask", ctypes.c_void_p)]
 
 
 class Stats(ctypes.Structure):
@@ -66,6 +70,9 @@ def lib():
         L.orc_score.argtypes = [f32, f32]
         L.orc_route_from_logits.restype = i32
         L.orc_route_from_logits.argtypes = [ctypes.POINTER(Cfg), vp, i32, vp, vp, vp]
+        L.orc_route_from_logits_vl.restype = i32
+        L.orc_route_from_logits_vl.argtypes = [ctypes.POINTER(Cfg), vp, i32, vp, vp, vp, vp, vp]
+        L.orc_scores.argtypes = [ctypes.POINTER(Cfg), vp, vp]
         L.orc_swiglu.restype = dbl
         L.orc_swiglu.argtypes = [dbl, dbl, dbl, vp]
         L.orc_expert_kquant.argtypes = [ctypes.POINTER(Cfg), vp, vp, vp, vp, vp, vp]
@@ -81,14 +88,16 @@ def _p(a):
     return None if a is None else a.ctypes.data
 
 
-def make_cfg(dim, inter, n_routed, topk, gate_temp=1.0, norm_topk_prob=True, route_scale=1.5, swiglu_limit=10.0):
-    return Cfg(dim, inter, n_routed, topk, gate_temp, int(bool(norm_topk_prob)), route_scale, swiglu_limit)
+def make_cfg(dim, inter, n_routed, topk, gate_temp=1.0, norm_topk_prob=True, route_scale=1.5, swiglu_limit=10.0,
+             score_func=SCORE_SQRTSOFTPLUS):
+    return Cfg(dim, inter, n_routed, topk, gate_temp, int(bool(norm_topk_prob)), route_scale, swiglu_limit,
+               int(score_func))
 
 
 def cfg_of(w) -> Cfg:
     """oracle config of a synth.workloads.Workload"""
     return make_cfg(w.dim, w.inter, w.n_routed, w.topk, w.gate_temp, w.norm_topk_prob, w.route_scale,
-                    w.swiglu_limit)
+                    w.swiglu_limit, getattr(w, "score_func", SCORE_SQRTSOFTPLUS))
 
 
 # ----------------------------------------------------------------- formats
@@ -170,15 +179,26 @@ def score(z: float, gate_temp: float = 1.0) -> float:
     return lib().orc_score(z, gate_temp)
 
 
-def route_from_logits(cfg: Cfg, logits: np.ndarray, bias: np.ndarray):
-    """(weights f32 [m, k], indices i32 [m, k], nan_keys)"""
+def route_from_logits(cfg: Cfg, logits: np.ndarray, bias: np.ndarray, bias_vl=None, image_mask=None):
+    """(weights f32 [m, k], indices i32 [m, k], nan_keys); tokens with a nonzero
+    image_mask entry pick with bias_vl"""
     z = np.ascontiguousarray(logits, dtype=np.float32)
     b = np.ascontiguousarray(bias, dtype=np.float32)
+    bv = None if bias_vl is None else np.ascontiguousarray(bias_vl, dtype=np.float32)
+    im = None if image_mask is None else np.ascontiguousarray(image_mask, dtype=np.uint8)
     m = z.shape[0]
     w = np.empty((m, cfg.topk), dtype=np.float32)
     idx = np.empty((m, cfg.topk), dtype=np.int32)
-    nan = lib().orc_route_from_logits(ctypes.byref(cfg), _p(z), m, _p(b), _p(w), _p(idx))
+    nan = lib().orc_route_from_logits_vl(ctypes.byref(cfg), _p(z), m, _p(b), _p(bv), _p(im), _p(w), _p(idx))
     return w, idx, nan
+
+
+def scores(cfg: Cfg, logits_row: np.ndarray) -> np.ndarray:
+    """f32 scores of one token's logits by the configuration's score function"""
+    z = np.ascontiguousarray(logits_row, dtype=np.float32)
+    s = np.empty(cfg.n_routed, dtype=np.float32)
+    lib().orc_scores(ctypes.byref(cfg), _p(z), _p(s))
+    return s
 
 
 def swiglu(g: float, u: float, limit: float) -> float:
@@ -211,7 +231,7 @@ class LayerResult:
 
 
 def moe_layer(cfg: Cfg, x, router_w, bias, experts, shared_kind, sh1, sh3, sh2, tokens=None, given_logits=None,
-              nthreads=None) -> LayerResult:
+              nthreads=None, bias_vl=None, image_mask=None) -> LayerResult:
     """One MoE layer on the CPU.
 
     experts: list of n_routed entries, each None or a (w1, w3, w2) tuple of uint8
@@ -234,8 +254,10 @@ def moe_layer(cfg: Cfg, x, router_w, bias, experts, shared_kind, sh1, sh3, sh2, 
             table[3 * e + j] = a.ctypes.data
     sh = [np.ascontiguousarray(s) for s in (sh1, sh3, sh2)]
     gl = None if given_logits is None else np.ascontiguousarray(given_logits, dtype=np.float32)
+    bv = None if bias_vl is None else np.ascontiguousarray(bias_vl, dtype=np.float32)
+    im = None if image_mask is None else np.ascontiguousarray(image_mask, dtype=np.uint8)
     L = Layer(_p(x), _p(router_w), _p(bias), _p(gl), ctypes.cast(table, ctypes.c_void_p), shared_kind,
-              _p(sh[0]), _p(sh[1]), _p(sh[2]))
+              _p(sh[0]), _p(sh[1]), _p(sh[2]), _p(bv), _p(im))
     if tokens is None:
         tok = None
         n_tok = m

@@ -25,7 +25,7 @@
  * (the "All 22 steps" equations, the Parameters table, the model.py
  * MoE/Gate/Expert listings and config.json).
  *
- * Readings of what the pages leave open (each is listed in the design notes):
+ * Readings of what the pages leave open:
  *   C-L1  Q2_K block, 84 B: scales[16] (low nibble scale, high nibble min),
  *         qs[64], fp16 d, fp16 dmin; element e = 128h + 32j + l (l < 32):
  *         q = (qs[32h + l] >> 2j) & 3, sub-block b = e / 16,
@@ -42,6 +42,12 @@
  *         the dequantised value is fp16(d) * q.
  *   C-R2  score s = f32 of sqrt(log1p(exp(t))) evaluated in f64 for
  *         t = z / gate_temp (f32) <= 20, and f32 sqrt(t) above 20.
+ *   C-R6  the sigmoid and softmax score functions (model.py Gate.forward)
+ *         are evaluated the same way: f64 from t = f32(z / gate_temp),
+ *         rounded once to f32; the softmax subtracts the largest t and sums
+ *         the experts in id order; a NaN logit makes every softmax score NaN.
+ *         Image tokens pick with bias_vl, and their weights stay the raw
+ *         scores as for every token.
  *   C-R3  ties on equal f32 keys go to the lower expert id; picks come out in
  *         descending key order.  C-R4: a NaN key ranks below every number and
  *         is counted.
@@ -201,6 +207,35 @@ float orc_score(float z, float gate_temp) {
   return (float)sqrt(log1p(exp((double)t)));
 }
 
+/* The scores of one token's logits z[N] by the configuration's score function
+ * ([MoE atlas] model.py Gate.forward: scores = linear(x, W) / gate_temp, then
+ * softmax over the experts, sigmoid, or sqrt(softplus)).  Every step is
+ * evaluated in f64 from t = f32(z / gate_temp) and rounded once to f32 (the
+ * reading C-R2 extends to the other two functions); the softmax takes the
+ * largest t as its shift and sums the experts in id order. */
+void orc_scores(const orc_cfg* c, const float* z, float* s) {
+  int N = c->n_routed;
+  if (c->score_func == ORC_SCORE_SIGMOID) {
+    for (int e = 0; e < N; ++e) {
+      float t = z[e] / c->gate_temp;
+      s[e] = (float)(1.0 / (1.0 + exp(-(double)t)));
+    }
+  } else if (c->score_func == ORC_SCORE_SOFTMAX) {
+    double mx = -INFINITY, sum = 0.0;
+    int any_nan = 0;
+    for (int e = 0; e < N; ++e) {
+      float t = z[e] / c->gate_temp;
+      if (isnan(t)) any_nan = 1;
+      else if (t > mx) mx = t;
+    }
+    for (int e = 0; e < N; ++e) sum += exp((double)(z[e] / c->gate_temp) - mx);
+    for (int e = 0; e < N; ++e)
+      s[e] = any_nan ? NAN : (float)(exp((double)(z[e] / c->gate_temp) - mx) / sum);
+  } else {
+    for (int e = 0; e < N; ++e) s[e] = orc_score(z[e], c->gate_temp);
+  }
+}
+
 /* a ranks before b: larger key first, NaN last, equal keys by lower id */
 static int ranks_before(float ka, int a, float kb, int b) {
   int na = isnan(ka), nb = isnan(kb);
@@ -219,8 +254,8 @@ int orc_route_token(const orc_cfg* c, const float* z, const float* bias, float* 
   float* s = (float*)malloc(sizeof(float) * N);
   float* key = (float*)malloc(sizeof(float) * N);
   int* order = (int*)malloc(sizeof(int) * N);
+  orc_scores(c, z, s);
   for (int e = 0; e < N; ++e) {
-    s[e] = orc_score(z[e], c->gate_temp);
     key[e] = s[e] + bias[e];
     if (isnan(key[e])) ++nan_keys;
     order[e] = e;
@@ -251,10 +286,20 @@ int orc_route_token(const orc_cfg* c, const float* z, const float* bias, float* 
 
 int orc_route_from_logits(const orc_cfg* c, const float* z, int m, const float* bias, float* w_out,
                           int32_t* idx_out) {
+  return orc_route_from_logits_vl(c, z, m, bias, NULL, NULL, w_out, idx_out);
+}
+
+/* The same with the image-token bias: a token whose image_mask entry is
+ * nonzero picks with bias_vl instead of bias ([MoE atlas] model.py
+ * Gate.forward, torch.where(image_mask, bias_vl, bias)). */
+int orc_route_from_logits_vl(const orc_cfg* c, const float* z, int m, const float* bias, const float* bias_vl,
+                             const uint8_t* image_mask, float* w_out, int32_t* idx_out) {
   int nan_keys = 0;
-  for (int t = 0; t < m; ++t)
-    nan_keys += orc_route_token(c, z + (size_t)t * c->n_routed, bias, w_out + (size_t)t * c->topk,
+  for (int t = 0; t < m; ++t) {
+    const float* b = (image_mask && bias_vl && image_mask[t]) ? bias_vl : bias;
+    nan_keys += orc_route_token(c, z + (size_t)t * c->n_routed, b, w_out + (size_t)t * c->topk,
                                 idx_out + (size_t)t * c->topk);
+  }
   return nan_keys;
 }
 
@@ -357,7 +402,8 @@ static int token_forward(const orc_cfg* c, const orc_layer* L, int t, double* ou
   float* z = (float*)malloc(sizeof(float) * N);
   if (L->given_logits) memcpy(z, L->given_logits + (size_t)t * N, sizeof(float) * N);
   else orc_router_logits(xt, 1, L->router_w, D, N, z);
-  *nan_keys += orc_route_token(c, z, L->bias, w, idx);
+  const float* bias = (L->image_mask && L->bias_vl && L->image_mask[t]) ? L->bias_vl : L->bias;
+  *nan_keys += orc_route_token(c, z, bias, w, idx);
   free(z);
 
   float* xf = (float*)malloc(sizeof(float) * D);

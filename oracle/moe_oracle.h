@@ -11,7 +11,12 @@ typedef struct {
   float gate_temp;
   int32_t norm_topk_prob;
   float route_scale, swiglu_limit;
+  int32_t score_func;              /* ORC_SCORE_*: the Gate's score function */
 } orc_cfg;
+
+/* [MoE atlas] model.py Gate.forward: score_func "sqrtsoftplus" (the default),
+ * "sigmoid" or "softmax" over the experts */
+enum { ORC_SCORE_SQRTSOFTPLUS = 0, ORC_SCORE_SIGMOID = 1, ORC_SCORE_SOFTMAX = 2 };
 
 enum { ORC_SHARED_BF16 = 0, ORC_SHARED_KQUANT = 1 };
 enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_MISSING_EXPERT = 2 };
@@ -26,6 +31,8 @@ typedef struct {
   const void* sh1;                 /* bf16 [inter, dim] or Q2_K */
   const void* sh3;                 /* bf16 [inter, dim] or Q2_K */
   const void* sh2;                 /* bf16 [dim, inter] or Q3_K */
+  const float* bias_vl;            /* optional f32 [n_routed]: the bias of image tokens */
+  const uint8_t* image_mask;       /* optional [m]: nonzero for tokens inside an image span */
 } orc_layer;
 
 typedef struct {
@@ -45,9 +52,12 @@ void orc_quantize_q8_1(const float* x, int n, uint8_t* out);
 void orc_dequant_q8_1(const uint8_t* q8, int n, double* out);
 void orc_router_logits(const uint16_t* x, int m, const uint16_t* W, int D, int N, float* z);
 float orc_score(float z, float gate_temp);
+void orc_scores(const orc_cfg* c, const float* z, float* s);
 int orc_route_token(const orc_cfg* c, const float* z, const float* bias, float* w_out, int32_t* idx_out);
 int orc_route_from_logits(const orc_cfg* c, const float* z, int m, const float* bias, float* w_out,
                           int32_t* idx_out);
+int orc_route_from_logits_vl(const orc_cfg* c, const float* z, int m, const float* bias, const float* bias_vl,
+                             const uint8_t* image_mask, float* w_out, int32_t* idx_out);
 double orc_swiglu(double g, double u, double limit, int* clipped);
 void orc_expert_kquant(const orc_cfg* c, const uint8_t* xq8, const uint8_t* w1, const uint8_t* w3,
                        const uint8_t* w2, double* E, int* clipped);

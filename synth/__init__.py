@@ -19,7 +19,7 @@ HOST_SO = os.path.join(_LIBDIR, "libsynth_host.so")
 GPU_SO = os.path.join(_LIBDIR, "libsynth_gpu.so")
 
 # tensor ids, mirroring synth_core.h
-T_X, T_ROUTER, T_BIAS, T_W1, T_W3, T_W2, T_SH1, T_SH3, T_SH2, T_OUTLIER, T_HOT = range(1, 12)
+T_X, T_ROUTER, T_BIAS, T_W1, T_W3, T_W2, T_SH1, T_SH3, T_SH2, T_OUTLIER, T_HOT, T_BIAS_VL, T_IMAGE = range(1, 14)
 
 Q2K_BYTES = 84   # bytes per Q2_K super-block of 256 weights
 Q3K_BYTES = 110  # bytes per Q3_K super-block of 256 weights

@@ -19,6 +19,8 @@ Recipe (all workloads):
           scale codes uniform; fp16 d ~ U(5e-4, 2e-3).
   shared  bf16 N(0, 0.02^2) w1 [inter, dim], w3 [inter, dim], w2 [dim, inter];
           or, in the m=8 workload, K-quant blocks drawn like the routed ones.
+  vision  (variants only) bias_vl f32 U(-0.1, 0.1) [n_routed] and an image
+          span: round(image_frac * m) consecutive tokens from a seeded start.
 Layer l of a workload draws every tensor from the stream key
 (seed, layer=l, tensor id, expert).
 """
@@ -29,8 +31,8 @@ import math
 
 import numpy as np
 
-from . import (Q2K_BYTES, Q3K_BYTES, T_BIAS, T_HOT, T_OUTLIER, T_ROUTER, T_SH1, T_SH2, T_SH3, T_W1, T_W2,
-               T_W3, T_X, key, normal_bf16, permutation, q2k_blocks, q3k_blocks, uniform_f32)
+from . import (Q2K_BYTES, Q3K_BYTES, T_BIAS, T_BIAS_VL, T_HOT, T_IMAGE, T_OUTLIER, T_ROUTER, T_SH1, T_SH2, T_SH3,
+               T_W1, T_W2, T_W3, T_X, key, normal_bf16, permutation, q2k_blocks, q3k_blocks, uniform_f32)
 
 SHARED_BF16 = 0
 SHARED_KQUANT = 1
@@ -55,6 +57,8 @@ class Workload:
     route_scale: float = 1.5
     swiglu_limit: float = 10.0
     seed: int = 0
+    score_func: int = 0          # 0 sqrt-softplus, 1 sigmoid, 2 softmax (model.py Gate.forward)
+    image_frac: float = 0.0      # share of the tokens inside an image span (they pick with bias_vl)
 
     # --- sizes of the raw expert blocks ---
     @property
@@ -124,6 +128,22 @@ def bias_f32(w: Workload, layer: int) -> np.ndarray:
     if hot.size:
         b[hot] = b[hot] + np.float32(w.hot_bias)
     return b
+
+
+def bias_vl_f32(w: Workload, layer: int) -> np.ndarray:
+    """the bias image tokens pick with"""
+    return uniform_f32(w.n_routed, key(w.seed, layer, T_BIAS_VL), -0.1, 0.1)
+
+
+def image_mask(w: Workload, layer: int) -> np.ndarray | None:
+    """uint8 [m]: 1 for the tokens of the image span; None without one"""
+    n = int(round(w.image_frac * w.m))
+    if n <= 0:
+        return None
+    start = int(permutation(w.m - n + 1, key(w.seed, layer, T_IMAGE))[0])
+    mask = np.zeros(w.m, dtype=np.uint8)
+    mask[start:start + n] = 1
+    return mask
 
 
 def expert_blocks(w: Workload, layer: int, e: int):

@@ -279,6 +279,132 @@ def test_routing_nan_key_ranks_last():
     assert idx[0].tolist() == [6, 5, 4]
 
 
+# ------------------------------------------- score-function and image-bias variants
+# model.py Gate.forward (the atlas page): scores = linear(x, W) / gate_temp, then
+# softmax over the experts, sigmoid, or sqrt(softplus); image tokens pick with bias_vl.
+
+def _cfg_sf(n, k, sf, temp=1.0, norm=True):
+    return oracle.make_cfg(256, 256, n, k, temp, norm, 1.5, 10.0, sf)
+
+
+def _f32_ulp(v):
+    return np.spacing(np.float32(abs(v)))
+
+
+def test_sigmoid_score_closed_forms():
+    c = _cfg_sf(8, 2, oracle.SCORE_SIGMOID)
+    z = np.array([0.0, 40.0, -40.0, 2.0, -2.0, 1.0, 4.0, 0.5], np.float32)
+    s = oracle.scores(c, z)
+    assert s[0] == 0.5                                      # logistic(0)
+    assert s[1] == 1.0                                      # 1 - e^-40 rounds to 1 in f32
+    assert abs(s[2] / math.exp(-40.0) - 1) < 1e-6            # e^-40 / (1 + e^-40)
+    assert abs((s[3] + s[4]) - 1.0) <= 2 * _f32_ulp(1.0)     # logistic(t) + logistic(-t) = 1
+    assert abs(s[5] - SIGMA1) <= _f32_ulp(SIGMA1)
+    # the temperature divides first: z / 2 = 0.5 at z = 1
+    c2 = _cfg_sf(8, 2, oracle.SCORE_SIGMOID, temp=2.0)
+    assert oracle.scores(c2, z)[5] == s[7]
+
+
+def test_softmax_score_closed_forms():
+    n = 16
+    c = _cfg_sf(n, 2, oracle.SCORE_SOFTMAX)
+    assert np.all(oracle.scores(c, np.full(n, 3.25, np.float32)) == np.float32(1.0 / n))
+    # one raised logit: e^a / (e^a + n - 1)
+    z = np.zeros(n, np.float32)
+    z[5] = 2.0
+    s = oracle.scores(c, z)
+    top = math.exp(2.0) / (math.exp(2.0) + n - 1)
+    assert abs(s[5] - top) <= _f32_ulp(top)
+    assert abs(s[0] - 1.0 / (math.exp(2.0) + n - 1)) <= _f32_ulp(s[0])
+    # shift invariance on integer logits (the shifted t are exact): same bits
+    zi = np.arange(n, dtype=np.float32) - 7
+    assert np.array_equal(oracle.scores(c, zi), oracle.scores(c, zi + 5))
+    # a NaN logit makes every softmax score NaN; all keys rank last, by id
+    zn = zi.copy()
+    zn[3] = np.nan
+    w, idx, nan = oracle.route_from_logits(c, zn[None, :], np.zeros(n, np.float32))
+    assert nan == n and idx[0].tolist() == [0, 1]
+
+
+@pytest.mark.parametrize("sf", [1, 2])
+def test_variant_scores_match_a_numpy_restatement(sf):
+    """The f64 formulas restated with numpy: within one f32 ulp (the two exp
+    implementations may differ in the last f64 bit)."""
+    rng = np.random.default_rng(11 + sf)
+    n = 384
+    c = _cfg_sf(n, 6, sf, temp=0.7)
+    for _ in range(8):
+        z = (rng.standard_normal(n) * 3).astype(np.float32)
+        t = (z / np.float32(0.7)).astype(np.float32).astype(np.float64)
+        ref = 1.0 / (1.0 + np.exp(-t)) if sf == 1 else np.exp(t - t.max()) / np.sum(np.exp(t - t.max()))
+        s = oracle.scores(c, z).astype(np.float64)
+        assert np.all(np.abs(s - ref) <= np.spacing(ref.astype(np.float32)).astype(np.float64) + 1e-45)
+
+
+@pytest.mark.parametrize("sf", [1, 2])
+def test_variant_routing_matches_brute_force_sort(sf):
+    rng = np.random.default_rng(5 + sf)
+    n, k, m = 384, 6, 32
+    z = rng.standard_normal((m, n)).astype(np.float32)
+    bias = rng.uniform(-0.1, 0.1, n).astype(np.float32) * (0.01 if sf == 2 else 1)
+    c = _cfg_sf(n, k, sf)
+    w, idx, _ = oracle.route_from_logits(c, z, bias)
+    for t in range(m):
+        s = oracle.scores(c, z[t])
+        key = (s + bias).astype(np.float32)
+        order = np.lexsort((np.arange(n), -key.astype(np.float64)))
+        assert idx[t].tolist() == order[:k].tolist()
+        g = s[order[:k]].astype(np.float32)
+        expect = (g / (np.float32(g.astype(np.float64).sum()) + np.float32(1e-20))) * np.float32(1.5)
+        np.testing.assert_allclose(w[t], expect, rtol=3e-7)
+    np.testing.assert_allclose(w.sum(axis=1), 1.5, rtol=2e-6)
+
+
+def test_image_tokens_pick_with_bias_vl():
+    rng = np.random.default_rng(21)
+    n, k, m = 64, 4, 12
+    c = _cfg_sf(n, k, oracle.SCORE_SQRTSOFTPLUS)
+    z = rng.standard_normal((m, n)).astype(np.float32)
+    bias = rng.uniform(-0.1, 0.1, n).astype(np.float32)
+    w0, i0, _ = oracle.route_from_logits(c, z, bias)
+    # no image token, or bias_vl equal to bias: nothing changes
+    w1, i1, _ = oracle.route_from_logits(c, z, bias, bias.copy(), np.ones(m, np.uint8))
+    w2, i2, _ = oracle.route_from_logits(c, z, bias, bias + 1, np.zeros(m, np.uint8))
+    assert np.array_equal(i0, i1) and np.array_equal(i0, i2)
+    assert np.array_equal(w0, w1) and np.array_equal(w0, w2)
+    # a bias_vl that lifts experts 3, 17, 40, 41 makes the image tokens pick exactly them;
+    # their weights are the raw scores of those picks (the bias never scales)
+    bvl = np.zeros(n, np.float32)
+    bvl[[3, 17, 40, 41]] = 100.0
+    mask = np.zeros(m, np.uint8)
+    mask[4:9] = 1
+    w3, i3, _ = oracle.route_from_logits(c, z, bias, bvl, mask)
+    for t in range(m):
+        if mask[t]:
+            assert sorted(i3[t].tolist()) == [3, 17, 40, 41]
+            s = oracle.scores(c, z[t])[i3[t]]
+            np.testing.assert_allclose(w3[t] / w3[t].sum(), s / s.sum(), rtol=1e-6)
+        else:
+            assert np.array_equal(i3[t], i0[t]) and np.array_equal(w3[t], w0[t])
+
+
+def test_layer_image_tokens_equal_the_layer_with_bias_vl():
+    w = _tiny().with_(m=6, image_frac=0.5)
+    L = _tiny_layer(w)
+    cfg = oracle.cfg_of(w)
+    bvl = W.bias_vl_f32(w, 0) * np.float32(20)  # strong enough to change picks
+    mask = W.image_mask(w, 0)
+    r = oracle.moe_layer(cfg, L["x"], L["router_w"], L["bias"], L["experts"], w.shared_kind, *L["shared"],
+                         bias_vl=bvl, image_mask=mask)
+    plain = oracle.moe_layer(cfg, L["x"], L["router_w"], L["bias"], L["experts"], w.shared_kind, *L["shared"])
+    vl = oracle.moe_layer(cfg, L["x"], L["router_w"], bvl, L["experts"], w.shared_kind, *L["shared"])
+    for t in range(w.m):
+        ref = vl if mask[t] else plain
+        assert np.array_equal(r.topk_idx[t], ref.topk_idx[t])
+        np.testing.assert_array_equal(r.out[t], ref.out[t])
+    assert np.any(vl.topk_idx[mask == 1] != plain.topk_idx[mask == 1])
+
+
 # -------------------------------------------------------------------- SwiGLU
 
 SIGMA1 = 0.7310585786300049   # logistic(1)
