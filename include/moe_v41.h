@@ -42,20 +42,29 @@ extern "C" {
 #endif
 
 /* Layer configuration; mirrors the metrale MoeV41Cfg struct (moe_v41.rs source)
- * plus two execution fields. */
+ * plus two execution fields and the DeepSeek Gate's score function. */
 typedef struct {
   int32_t dim;              /* D, model width: multiple of 256, <= 7680 */
   int32_t inter;            /* I, expert hidden width: multiple of 256, <= 7680 */
   int32_t n_routed;         /* N, routed experts: 1..1024 */
   int32_t topk;             /* k, experts per token: 1..min(N, 16) */
-  float gate_temp;          /* > 0; the logit is divided by it before softplus */
+  float gate_temp;          /* > 0; the logit is divided by it before the score function */
   int32_t norm_topk_prob;   /* non-zero: renormalise the k weights (when k > 1) */
   float route_scale;        /* weights are multiplied by it */
   float swiglu_limit;       /* L; <= 0 disables both clamps */
   int32_t max_tokens;       /* largest m the workspace is sized for: 1..65536 */
   int32_t path;             /* MOE_PATH_*: which kernel family runs */
   uint32_t wait_timeout_us; /* bound of every in-kernel wait; 0 = 2,000,000 */
+  int32_t score_func;       /* MOE_SCORE_*; 0 = sqrt(softplus), the moe_v41 default */
 } moe_v41_cfg;
+
+/* Score functions of the DeepSeek V4.1 Gate (atlas page "Mixture of experts",
+ * model.py Gate.forward), on t = f32(logit / gate_temp).  Each score is the
+ * f64 evaluation of the formula rounded once to f32:
+ *   MOE_SCORE_SQRTSOFTPLUS  sqrt(softplus(t)), softplus(t) = t above 20
+ *   MOE_SCORE_SIGMOID       1 / (1 + exp(-t))
+ *   MOE_SCORE_SOFTMAX       exp(t - max t) / sum over the experts of the same */
+enum { MOE_SCORE_SQRTSOFTPLUS = 0, MOE_SCORE_SIGMOID = 1, MOE_SCORE_SOFTMAX = 2 };
 
 enum {
   MOE_PATH_AUTO = 0,    /* decode kernels for m <= 8, prefill kernels above */
@@ -111,12 +120,25 @@ MOE_API int moe_v41_quantize_q8_1(const void* x, int x_is_f32, int rows, int col
 MOE_API int moe_v41_select_from_logits(const moe_v41_cfg* cfg, const float* logits, int m, const float* bias,
                                float* topk_w, int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream);
 
+/* The same with the image-token bias of the DeepSeek Gate (model.py
+ * Gate.forward, torch.where(image_mask, bias_vl, bias)): token t picks with
+ * bias_vl when image_mask[t] is non-zero.  bias_vl f32 [n_routed] and
+ * image_mask uint8 [m] are DEVICE arrays; either NULL means no image token.
+ * The weights stay the raw scores for every token.  The _vl forms of route
+ * and forward below take the same two arguments after bias. */
+MOE_API int moe_v41_select_from_logits_vl(const moe_v41_cfg* cfg, const float* logits, int m, const float* bias,
+                                          const float* bias_vl, const uint8_t* image_mask, float* topk_w,
+                                          int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream);
+
 /* Router logits and routing for m tokens (the metrale route call, with the
  * selection on the device): x bf16 [m, dim], router_w bf16 [n_routed, dim]
  * (16-B aligned), bias f32 [n_routed].  logits_out (may be NULL) receives the
  * f32 logits [m, n_routed]. */
 MOE_API int moe_v41_route(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w, const float* bias,
                   float* logits_out, float* topk_w, int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream);
+MOE_API int moe_v41_route_vl(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w, const float* bias,
+                             const float* bias_vl, const uint8_t* image_mask, float* logits_out, float* topk_w,
+                             int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream);
 
 /* One MoE layer forward for m tokens (the metrale MoeV41::forward call, all
  * experts resident).  Up to eight tokens run the decode kernels (one
@@ -142,6 +164,11 @@ MOE_API int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const 
                     const uint64_t* expert_ptrs, int shared_kind, const void* sh_w1, const void* sh_w3,
                     const void* sh_w2, float* out, float* topk_w, int32_t* topk_idx, float* logits_out, void* ws,
                     size_t ws_bytes, void* stream);
+MOE_API int moe_v41_forward_vl(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w, const float* bias,
+                               const float* bias_vl, const uint8_t* image_mask, const uint64_t* expert_ptrs,
+                               int shared_kind, const void* sh_w1, const void* sh_w3, const void* sh_w2, float* out,
+                               float* topk_w, int32_t* topk_idx, float* logits_out, void* ws, size_t ws_bytes,
+                               void* stream);
 
 /* Bytes of the fixed scratch array behind moe_v41_forward_noalloc (512 KiB).
  * Each GPU that loads this library holds it until the process exits. */

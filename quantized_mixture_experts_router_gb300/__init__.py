@@ -14,6 +14,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 SO = os.path.join(_HERE, "_lib", "libmoe_v41.so")
 
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
+MOE_SCORE_SQRTSOFTPLUS, MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1, 2
 MOE_SHARED_BF16, MOE_SHARED_KQUANT = 0, 1
 MOE_OK, MOE_ERR_ARG, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = 0, 1, 2, 3, 4
 MOE_STATUS_NAN_KEY, MOE_STATUS_MISSING_EXPERT, MOE_STATUS_TIMEOUT = 1, 2, 4
@@ -29,7 +30,7 @@ class moe_v41_cfg(ctypes.Structure):
     _fields_ = [("dim", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_routed", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("gate_temp", ctypes.c_float), ("norm_topk_prob", ctypes.c_int32),
                 ("route_scale", ctypes.c_float), ("swiglu_limit", ctypes.c_float), ("max_tokens", ctypes.c_int32),
-                ("path", ctypes.c_int32), ("wait_timeout_us", ctypes.c_uint32)]
+                ("path", ctypes.c_int32), ("wait_timeout_us", ctypes.c_uint32), ("score_func", ctypes.c_int32)]
 
 
 _lib = None
@@ -49,6 +50,10 @@ def lib():
         L.moe_v41_select_from_logits.argtypes = [cfgp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.moe_v41_route.argtypes = [cfgp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.moe_v41_forward.argtypes = [cfgp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.moe_v41_select_from_logits_vl.argtypes = [cfgp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.moe_v41_route_vl.argtypes = [cfgp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.moe_v41_forward_vl.argtypes = [cfgp, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                         vp]
         L.moe_v41_read_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32), i32]
         L.moe_v41_forward_noalloc.argtypes = [cfgp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_v41_kernel_launches.argtypes = [cfgp, i32, i32]
@@ -56,7 +61,8 @@ def lib():
         L.moe_v41_strerror.restype = ctypes.c_char_p
         L.moe_v41_strerror.argtypes = [i32]
         for f in ("moe_v41_workspace_init", "moe_v41_quantize_q8_1", "moe_v41_select_from_logits", "moe_v41_route",
-                  "moe_v41_forward", "moe_v41_read_status", "moe_v41_forward_noalloc"):
+                  "moe_v41_forward", "moe_v41_read_status", "moe_v41_forward_noalloc",
+                  "moe_v41_select_from_logits_vl", "moe_v41_route_vl", "moe_v41_forward_vl"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -94,9 +100,9 @@ def _check(rc: int, what: str):
 
 
 def make_cfg(dim, inter, n_routed, topk, gate_temp=1.0, norm_topk_prob=True, route_scale=1.5, swiglu_limit=10.0,
-             max_tokens=1, path=MOE_PATH_AUTO, wait_timeout_us=0) -> moe_v41_cfg:
+             max_tokens=1, path=MOE_PATH_AUTO, wait_timeout_us=0, score_func=MOE_SCORE_SQRTSOFTPLUS) -> moe_v41_cfg:
     return moe_v41_cfg(dim, inter, n_routed, topk, gate_temp, int(bool(norm_topk_prob)), route_scale, swiglu_limit,
-                       max_tokens, path, wait_timeout_us)
+                       max_tokens, path, wait_timeout_us, score_func)
 
 
 def moe_v41_workspace_bytes(cfg: moe_v41_cfg) -> int:
@@ -117,6 +123,18 @@ def moe_v41_select_from_logits(cfg, logits, m, bias, topk_w, topk_idx, ws, strea
                                             _p(ws), _nbytes(ws), _s(stream)), "moe_v41_select_from_logits")
 
 
+def moe_v41_select_from_logits_vl(cfg, logits, m, bias, bias_vl, image_mask, topk_w, topk_idx, ws, stream=None):
+    _check(lib().moe_v41_select_from_logits_vl(ctypes.byref(cfg), _p(logits), m, _p(bias), _p(bias_vl),
+                                               _p(image_mask), _p(topk_w), _p(topk_idx), _p(ws), _nbytes(ws),
+                                               _s(stream)), "moe_v41_select_from_logits_vl")
+
+
+def moe_v41_route_vl(cfg, x, m, router_w, bias, bias_vl, image_mask, logits_out, topk_w, topk_idx, ws, stream=None):
+    _check(lib().moe_v41_route_vl(ctypes.byref(cfg), _p(x), m, _p(router_w), _p(bias), _p(bias_vl), _p(image_mask),
+                                  _p(logits_out), _p(topk_w), _p(topk_idx), _p(ws), _nbytes(ws), _s(stream)),
+           "moe_v41_route_vl")
+
+
 def moe_v41_route(cfg, x, m, router_w, bias, logits_out, topk_w, topk_idx, ws, stream=None):
     _check(lib().moe_v41_route(ctypes.byref(cfg), _p(x), m, _p(router_w), _p(bias), _p(logits_out), _p(topk_w),
                                _p(topk_idx), _p(ws), _nbytes(ws), _s(stream)), "moe_v41_route")
@@ -127,6 +145,14 @@ def moe_v41_forward(cfg, x, m, router_w, bias, expert_ptrs, shared_kind, sh_w1, 
     _check(lib().moe_v41_forward(ctypes.byref(cfg), _p(x), m, _p(router_w), _p(bias), _p(expert_ptrs), shared_kind,
                                  _p(sh_w1), _p(sh_w3), _p(sh_w2), _p(out), _p(topk_w), _p(topk_idx), _p(logits_out),
                                  _p(ws), _nbytes(ws), _s(stream)), "moe_v41_forward")
+
+
+def moe_v41_forward_vl(cfg, x, m, router_w, bias, bias_vl, image_mask, expert_ptrs, shared_kind, sh_w1, sh_w3, sh_w2,
+                       out, topk_w, topk_idx, logits_out, ws, stream=None):
+    _check(lib().moe_v41_forward_vl(ctypes.byref(cfg), _p(x), m, _p(router_w), _p(bias), _p(bias_vl), _p(image_mask),
+                                    _p(expert_ptrs), shared_kind, _p(sh_w1), _p(sh_w3), _p(sh_w2), _p(out),
+                                    _p(topk_w), _p(topk_idx), _p(logits_out), _p(ws), _nbytes(ws), _s(stream)),
+           "moe_v41_forward_vl")
 
 
 NOALLOC_SCRATCH_BYTES = 512 << 10

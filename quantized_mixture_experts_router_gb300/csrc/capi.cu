@@ -18,6 +18,7 @@ int check_cfg(const moe_v41_cfg* c) {
   if (!(c->gate_temp > 0.0f)) return MOE_ERR_ARG;
   if (c->max_tokens < 1 || c->max_tokens > 65536) return MOE_ERR_ARG;
   if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_PREFILL) return MOE_ERR_ARG;
+  if (c->score_func < MOE_SCORE_SQRTSOFTPLUS || c->score_func > MOE_SCORE_SOFTMAX) return MOE_ERR_ARG;
   return MOE_OK;
 }
 
@@ -46,12 +47,14 @@ bool use_decode(const moe_v41_cfg* c, int m) {
 }
 
 RouteParams route_params(const moe_v41_cfg* c, const void* x, int m, const void* router_w, const float* bias,
-                         float* logits, float* topk_w, int32_t* topk_idx, uint8_t* ws, const WsLayout& L) {
+                         const float* bias_vl, const uint8_t* image_mask, float* logits, float* topk_w,
+                         int32_t* topk_idx, uint8_t* ws, const WsLayout& L) {
   RouteParams p{};
   p.x = static_cast<const uint16_t*>(x);
   p.router_w = static_cast<const uint16_t*>(router_w);
-  p.bias = bias;
+  p.bias = bias; p.bias_vl = bias_vl; p.image_mask = image_mask;
   p.m = m; p.D = c->dim; p.N = c->n_routed; p.k = c->topk; p.norm = c->norm_topk_prob != 0;
+  p.score_func = c->score_func;
   p.gate_temp = c->gate_temp; p.route_scale = c->route_scale;
   p.logits = logits ? logits : reinterpret_cast<float*>(ws + L.logits);
   p.topk_w = topk_w; p.topk_idx = topk_idx;
@@ -62,11 +65,13 @@ RouteParams route_params(const moe_v41_cfg* c, const void* x, int m, const void*
 }
 
 PrefillParams prefill_params(const moe_v41_cfg* c, const void* x, int m, const void* router_w, const float* bias,
-                             const uint64_t* expert_ptrs, int shared_kind, const void* sh1, const void* sh3,
-                             const void* sh2, float* out, float* topk_w, int32_t* topk_idx, float* logits,
-                             uint8_t* ws, const WsLayout& L) {
+                             const float* bias_vl, const uint8_t* image_mask, const uint64_t* expert_ptrs,
+                             int shared_kind, const void* sh1, const void* sh3, const void* sh2, float* out,
+                             float* topk_w, int32_t* topk_idx, float* logits, uint8_t* ws, const WsLayout& L) {
   PrefillParams p{};
   p.m = m; p.D = c->dim; p.I = c->inter; p.N = c->n_routed; p.k = c->topk; p.norm = c->norm_topk_prob != 0;
+  p.score_func = c->score_func;
+  p.bias_vl = bias_vl; p.image_mask = image_mask;
   p.gate_temp = c->gate_temp; p.route_scale = c->route_scale; p.swiglu_limit = c->swiglu_limit;
   p.shared_kind = shared_kind;
   p.x = static_cast<const uint16_t*>(x);
@@ -108,13 +113,21 @@ int moe_v41_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols, void*
 
 int moe_v41_select_from_logits(const moe_v41_cfg* cfg, const float* logits, int m, const float* bias,
                                float* topk_w, int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream) {
+  return moe_v41_select_from_logits_vl(cfg, logits, m, bias, nullptr, nullptr, topk_w, topk_idx, ws, ws_bytes,
+                                       stream);
+}
+
+int moe_v41_select_from_logits_vl(const moe_v41_cfg* cfg, const float* logits, int m, const float* bias,
+                                  const float* bias_vl, const uint8_t* image_mask, float* topk_w,
+                                  int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_cfg(cfg);
   if (rc) return rc;
   if (!logits || !bias || !topk_w || !topk_idx || m < 1 || m > cfg->max_tokens) return MOE_ERR_ARG;
   if ((rc = check_ws(cfg, ws, ws_bytes))) return rc;
   const WsLayout L = ws_layout(*cfg);
   SelectParams p{};
-  p.logits = logits; p.bias = bias; p.m = m; p.N = cfg->n_routed; p.k = cfg->topk;
+  p.logits = logits; p.bias = bias; p.bias_vl = bias_vl; p.image_mask = image_mask;
+  p.m = m; p.N = cfg->n_routed; p.k = cfg->topk; p.score_func = cfg->score_func;
   p.norm = cfg->norm_topk_prob != 0; p.gate_temp = cfg->gate_temp; p.route_scale = cfg->route_scale;
   p.topk_w = topk_w; p.topk_idx = topk_idx;
   p.ctrl = reinterpret_cast<Ctrl*>(static_cast<uint8_t*>(ws) + L.ctrl);
@@ -123,6 +136,13 @@ int moe_v41_select_from_logits(const moe_v41_cfg* cfg, const float* logits, int 
 
 int moe_v41_route(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w, const float* bias,
                   float* logits_out, float* topk_w, int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream) {
+  return moe_v41_route_vl(cfg, x, m, router_w, bias, nullptr, nullptr, logits_out, topk_w, topk_idx, ws, ws_bytes,
+                          stream);
+}
+
+int moe_v41_route_vl(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w, const float* bias,
+                     const float* bias_vl, const uint8_t* image_mask, float* logits_out, float* topk_w,
+                     int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_cfg(cfg);
   if (rc) return rc;
   if (!x || !router_w || !bias || !topk_w || !topk_idx || m < 1 || m > cfg->max_tokens) return MOE_ERR_ARG;
@@ -131,11 +151,11 @@ int moe_v41_route(const moe_v41_cfg* cfg, const void* x, int m, const void* rout
   const WsLayout L = ws_layout(*cfg);
   uint8_t* w = static_cast<uint8_t*>(ws);
   if (m <= DECODE_MAX_M && cfg->path != MOE_PATH_PREFILL) {
-    RouteParams p = route_params(cfg, x, m, router_w, bias, logits_out, topk_w, topk_idx, w, L);
+    RouteParams p = route_params(cfg, x, m, router_w, bias, bias_vl, image_mask, logits_out, topk_w, topk_idx, w, L);
     return launch_route_decode(p, (cudaStream_t)stream);
   }
-  PrefillParams p = prefill_params(cfg, x, m, router_w, bias, nullptr, MOE_SHARED_BF16, nullptr, nullptr, nullptr,
-                                   nullptr, topk_w, topk_idx, logits_out, w, L);
+  PrefillParams p = prefill_params(cfg, x, m, router_w, bias, bias_vl, image_mask, nullptr, MOE_SHARED_BF16, nullptr,
+                                   nullptr, nullptr, nullptr, topk_w, topk_idx, logits_out, w, L);
   return launch_prefill_route(p, (cudaStream_t)stream);
 }
 
@@ -143,6 +163,14 @@ int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const void* ro
                     const uint64_t* expert_ptrs, int shared_kind, const void* sh_w1, const void* sh_w3,
                     const void* sh_w2, float* out, float* topk_w, int32_t* topk_idx, float* logits_out, void* ws,
                     size_t ws_bytes, void* stream) {
+  return moe_v41_forward_vl(cfg, x, m, router_w, bias, nullptr, nullptr, expert_ptrs, shared_kind, sh_w1, sh_w3,
+                            sh_w2, out, topk_w, topk_idx, logits_out, ws, ws_bytes, stream);
+}
+
+int moe_v41_forward_vl(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w, const float* bias,
+                       const float* bias_vl, const uint8_t* image_mask, const uint64_t* expert_ptrs, int shared_kind,
+                       const void* sh_w1, const void* sh_w3, const void* sh_w2, float* out, float* topk_w,
+                       int32_t* topk_idx, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_cfg(cfg);
   if (rc) return rc;
   if (!x || !router_w || !bias || !expert_ptrs || !sh_w1 || !sh_w3 || !sh_w2 || !out || !topk_w || !topk_idx)
@@ -157,8 +185,8 @@ int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const void* ro
   cudaStream_t s = (cudaStream_t)stream;
   if (!use_decode(cfg, m)) {
     if (!prefill_possible(*cfg)) return MOE_ERR_ARG;
-    PrefillParams p = prefill_params(cfg, x, m, router_w, bias, expert_ptrs, shared_kind, sh_w1, sh_w3, sh_w2, out,
-                                     topk_w, topk_idx, logits_out, w, L);
+    PrefillParams p = prefill_params(cfg, x, m, router_w, bias, bias_vl, image_mask, expert_ptrs, shared_kind, sh_w1,
+                                     sh_w3, sh_w2, out, topk_w, topk_idx, logits_out, w, L);
     return launch_prefill(p, s);
   }
   if (m > DECODE_MAX_M) return MOE_ERR_ARG;
@@ -168,12 +196,12 @@ int moe_v41_forward(const moe_v41_cfg* cfg, const void* x, int m, const void* ro
   if (!decode_fits(cfg->dim, cfg->inter)) return MOE_ERR_ARG;
   DecodeParams dp{};
   dp.m = m; dp.D = cfg->dim; dp.I = cfg->inter; dp.N = cfg->n_routed; dp.k = cfg->topk;
-  dp.norm = cfg->norm_topk_prob != 0;
+  dp.norm = cfg->norm_topk_prob != 0; dp.score_func = cfg->score_func;
   dp.gate_temp = cfg->gate_temp; dp.route_scale = cfg->route_scale; dp.swiglu_limit = cfg->swiglu_limit;
   dp.shared_kind = shared_kind;
   dp.x = static_cast<const uint16_t*>(x);
   dp.router_w = static_cast<const uint16_t*>(router_w);
-  dp.bias = bias;
+  dp.bias = bias; dp.bias_vl = bias_vl; dp.image_mask = image_mask;
   dp.expert_ptrs = reinterpret_cast<const unsigned long long*>(expert_ptrs);
   dp.sh1 = static_cast<const uint8_t*>(sh_w1);
   dp.sh3 = static_cast<const uint8_t*>(sh_w3);

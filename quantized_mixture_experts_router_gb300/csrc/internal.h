@@ -9,7 +9,9 @@ namespace moe {
 struct SelectParams {
   const float* logits;  // [m, N]
   const float* bias;    // [N]
-  int m, N, k, norm;
+  const float* bias_vl;        // [N] or NULL: the bias of image tokens
+  const uint8_t* image_mask;   // [m] or NULL: nonzero marks an image token
+  int m, N, k, norm, score_func;
   float gate_temp, route_scale;
   float* topk_w;
   int* topk_idx;
@@ -20,7 +22,9 @@ struct RouteParams {
   const uint16_t* x;         // bf16 [m, D]
   const uint16_t* router_w;  // bf16 [N, D]
   const float* bias;
-  int m, D, N, k, norm;
+  const float* bias_vl;      // [N] or NULL
+  const uint8_t* image_mask; // [m] or NULL
+  int m, D, N, k, norm, score_func;
   float gate_temp, route_scale;
   float* logits;             // [m, N]
   float* topk_w;
@@ -31,12 +35,14 @@ struct RouteParams {
 };
 
 struct DecodeParams {
-  int m, D, I, N, k, norm;
+  int m, D, I, N, k, norm, score_func;
   float gate_temp, route_scale, swiglu_limit;
   int shared_kind;
   const uint16_t* x;         // bf16 [m, D]
   const uint16_t* router_w;  // bf16 [N, D]
   const float* bias;         // [N]
+  const float* bias_vl;      // [N] or NULL: the bias of image tokens
+  const uint8_t* image_mask; // [m] or NULL: nonzero marks an image token
   const unsigned long long* expert_ptrs;  // [N][3]
   const uint8_t* sh1;
   const uint8_t* sh3;
@@ -59,12 +65,14 @@ struct DecodeParams {
 };
 
 struct PrefillParams {
-  int m, D, I, N, k, norm;
+  int m, D, I, N, k, norm, score_func;
   float gate_temp, route_scale, swiglu_limit;
   int shared_kind;
   const uint16_t* x;         // bf16 [m, D]
   const uint16_t* router_w;  // bf16 [N, D]
   const float* bias;         // [N]
+  const float* bias_vl;      // [N] or NULL
+  const uint8_t* image_mask; // [m] or NULL
   const unsigned long long* expert_ptrs;  // [N][3]
   const uint8_t* sh1;
   const uint8_t* sh3;

@@ -413,12 +413,14 @@ __device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t 
   for (int t = 0; t < p.m; ++t) {
     float* wo = writer ? p.topk_w + (size_t)t * p.k : pk_w + t * p.k;
     int* io = writer ? p.topk_idx + (size_t)t * p.k : pk_id + t * p.k;
-    if (p.N <= 384)
-      route_token_warp_r12(p.logits + (size_t)t * p.N, p.sk + (size_t)t * p.N, p.bias, p.N, p.k, p.gate_temp,
-                           p.norm, p.route_scale, wo, io, status, scratch, pk_id + t * p.k, pk_w + t * p.k);
+    const float* bt = token_bias(p.bias, p.bias_vl, p.image_mask, t);
+    if (p.N <= 384 && p.score_func != MOE_SCORE_SOFTMAX)
+      route_token_warp_r12(p.logits + (size_t)t * p.N, p.sk + (size_t)t * p.N, bt, p.N, p.k, p.gate_temp,
+                           p.score_func, p.norm, p.route_scale, wo, io, status, scratch, pk_id + t * p.k,
+                           pk_w + t * p.k);
     else
-      route_token_warp(p.logits + (size_t)t * p.N, p.sk + (size_t)t * p.N, p.bias, p.N, p.k, p.gate_temp, p.norm,
-                       p.route_scale, wo, io, status, scratch, pk_id + t * p.k, pk_w + t * p.k);
+      route_token_warp(p.logits + (size_t)t * p.N, p.sk + (size_t)t * p.N, bt, p.N, p.k, p.gate_temp, p.score_func,
+                       p.norm, p.route_scale, wo, io, status, scratch, pk_id + t * p.k, pk_w + t * p.k);
   }
   // the expert pointer table: the block's copy when there is one
   const unsigned long long* eptr = p.expert_ptrs;
@@ -525,7 +527,8 @@ __device__ __noinline__ void task_local(const DecodeParams& p, Ctl& C, int part,
 }
 
 // router row e (stage offset st) against every token -> the logit and the
-// fast (score, key) pair the selection starts from
+// fast (score, key) pair the selection starts from (none for the softmax,
+// whose scores need every logit)
 __device__ __noinline__ void task_router(const DecodeParams& p, Ctl& C, uint32_t st, int e, uint64_t deadline) {
   const int lane = threadIdx.x & 31;
   require(p, C, RQ_XB | RQ_BIAS, deadline);
@@ -536,9 +539,13 @@ __device__ __noinline__ void task_router(const DecodeParams& p, Ctl& C, uint32_t
                              : bf16_rows_dot<1, false>(st, 0u, 0u,
                                                        reinterpret_cast<const uint8_t*>(p.x + (size_t)t * p.D), p.D / 8);
     if (lane == 0) {
-      const float sc = score_fast(s.x, p.gate_temp);
       p.logits[(size_t)t * p.N + e] = s.x;
-      p.sk[(size_t)t * p.N + e] = make_float2(sc, __fadd_rn(sc, bias[e]));
+      if (p.score_func != MOE_SCORE_SOFTMAX) {
+        // image tokens key on bias_vl (read from global memory)
+        const float* bt = (p.bias_vl && p.image_mask && __ldg(p.image_mask + t)) ? p.bias_vl : bias;
+        const float sc = score_fast(s.x, p.gate_temp, p.score_func);
+        p.sk[(size_t)t * p.N + e] = make_float2(sc, __fadd_rn(sc, bt[e]));
+      }
     }
   }
 }

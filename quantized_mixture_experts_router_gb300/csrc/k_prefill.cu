@@ -873,7 +873,8 @@ int route_steps(const PrefillParams& p, cudaStream_t s) {
   int rc = launch_gemm<A_BF16, 1, false, E_F32, PF_TN, 4, 4, 1, NP_BF, B_TILED>(g, grid, s);
   if (rc) return rc;
   SelectParams sp{};
-  sp.logits = p.logits; sp.bias = p.bias; sp.m = p.m; sp.N = p.N; sp.k = p.k; sp.norm = p.norm;
+  sp.logits = p.logits; sp.bias = p.bias; sp.bias_vl = p.bias_vl; sp.image_mask = p.image_mask;
+  sp.m = p.m; sp.N = p.N; sp.k = p.k; sp.norm = p.norm; sp.score_func = p.score_func;
   sp.gate_temp = p.gate_temp; sp.route_scale = p.route_scale; sp.topk_w = p.topk_w; sp.topk_idx = p.topk_idx;
   sp.ctrl = p.ctrl;
   return launch_select(sp, s);

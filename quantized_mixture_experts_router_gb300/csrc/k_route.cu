@@ -7,7 +7,8 @@
 // scores sqrt(softplus(logit / gate_temp)), keys score + bias, stable
 // descending order with ties to the lower id, weights the unbiased scores
 // renormalised when norm_topk_prob and topk > 1, times route_scale);
-// DeepSeek V4.1 atlas "Mixture of experts", model.py Gate.forward.
+// DeepSeek V4.1 atlas "Mixture of experts", model.py Gate.forward (sigmoid
+// and softmax scores; bias_vl for image tokens).
 #include "internal.h"
 #include "select.cuh"
 
@@ -32,10 +33,11 @@ __global__ void k_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols,
 __global__ void k_select(SelectParams p) {
   extern __shared__ __align__(16) float sel_scratch[];
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  float* scratch = sel_scratch + (size_t)(threadIdx.x >> 5) * 3 * p.N;
+  float* scratch = sel_scratch + (size_t)(threadIdx.x >> 5) * (select_scratch_bytes(p.N) / 4);
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < p.m; t += warps)
-    route_token_warp(p.logits + (size_t)t * p.N, nullptr, p.bias, p.N, p.k, p.gate_temp, p.norm, p.route_scale,
-                     p.topk_w + (size_t)t * p.k, p.topk_idx + (size_t)t * p.k, &p.ctrl->status, scratch);
+    route_token_warp(p.logits + (size_t)t * p.N, nullptr, token_bias(p.bias, p.bias_vl, p.image_mask, t), p.N, p.k,
+                     p.gate_temp, p.score_func, p.norm, p.route_scale, p.topk_w + (size_t)t * p.k,
+                     p.topk_idx + (size_t)t * p.k, &p.ctrl->status, scratch);
 }
 
 // ---------------------------------------------- router + selection (m <= 8)
@@ -113,9 +115,10 @@ __global__ void __launch_bounds__(256) k_route_decode(RouteParams p) {
   extern __shared__ __align__(16) float sel_scratch[];
   const int warp = threadIdx.x >> 5;
   if (warp < p.m)
-    route_token_warp(p.logits + (size_t)warp * p.N, nullptr, p.bias, p.N, p.k, p.gate_temp, p.norm, p.route_scale,
-                     p.topk_w + (size_t)warp * p.k, p.topk_idx + (size_t)warp * p.k, &p.ctrl->status,
-                     sel_scratch + (size_t)warp * 3 * p.N);
+    route_token_warp(p.logits + (size_t)warp * p.N, nullptr, token_bias(p.bias, p.bias_vl, p.image_mask, warp), p.N,
+                     p.k, p.gate_temp, p.score_func, p.norm, p.route_scale, p.topk_w + (size_t)warp * p.k,
+                     p.topk_idx + (size_t)warp * p.k, &p.ctrl->status,
+                     sel_scratch + (size_t)warp * (select_scratch_bytes(p.N) / 4));
 }
 
 // ------------------------------------------------------------- launchers

@@ -49,6 +49,7 @@ extern "C" int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, in
     return MOE_ERR_ARG;
   if (!(c.gate_temp > 0.0f) || c.max_tokens < 1 || c.max_tokens > DECODE_MAX_M) return MOE_ERR_ARG;
   if (c.path == MOE_PATH_PREFILL) return MOE_ERR_ARG;
+  if (c.score_func < MOE_SCORE_SQRTSOFTPLUS || c.score_func > MOE_SCORE_SOFTMAX) return MOE_ERR_ARG;
   if (m < 1 || m > c.max_tokens) return MOE_ERR_ARG;
   if (!x || !router_w || !bias || !expert_ptrs || !sh_w1 || !sh_w3 || !sh_w2 || !out || !topk_w || !topk_idx)
     return MOE_ERR_ARG;
@@ -74,7 +75,7 @@ extern "C" int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, in
 
   DecodeParams dp{};
   dp.m = m; dp.D = c.dim; dp.I = c.inter; dp.N = c.n_routed; dp.k = c.topk;
-  dp.norm = c.norm_topk_prob != 0;
+  dp.norm = c.norm_topk_prob != 0; dp.score_func = c.score_func;
   dp.gate_temp = c.gate_temp; dp.route_scale = c.route_scale; dp.swiglu_limit = c.swiglu_limit;
   dp.shared_kind = shared_kind;
   dp.x = static_cast<const uint16_t*>(x);

@@ -15,8 +15,8 @@ import numpy as np
 import torch
 
 from . import (Q2K_BYTES, Q3K_BYTES, T_ROUTER, T_SH1, T_SH2, T_SH3, T_W1, T_W2, T_W3, T_X, gpu_lib, key)
-from .workloads import (SHARED_BF16, Workload, bias_f32, expert_blocks, router_bf16, row_scale, shared_weights,
-                        x_bf16)
+from .workloads import (SHARED_BF16, Workload, bias_f32, bias_vl_f32, expert_blocks, image_mask, router_bf16,
+                        row_scale, shared_weights, x_bf16)
 
 ALIGN = 256
 
@@ -45,6 +45,8 @@ class DeviceLayer:
     sh1: torch.Tensor
     sh3: torch.Tensor
     sh2: torch.Tensor
+    bias_vl: torch.Tensor | None = None     # f32 [n_routed]: the bias of image tokens
+    image_mask: torch.Tensor | None = None  # uint8 [m]: 1 for image tokens
 
 
 def _stream():
@@ -142,7 +144,12 @@ def stage_layer(w: Workload, layer: int, device="cuda", experts_on_gpu: bool = T
     else:
         s1, s3, s2 = shared_weights(w, layer)
         sh1, sh3, sh2 = (_bits_to_dev(a, device) for a in (s1, s3, s2))
-    return DeviceLayer(w, layer, x, router, bias, experts, ptrs, sh1, sh3, sh2)
+    bias_vl = mask = None
+    im = image_mask(w, layer)
+    if im is not None:
+        bias_vl = torch.from_numpy(bias_vl_f32(w, layer)).to(device)
+        mask = torch.from_numpy(im).to(device)
+    return DeviceLayer(w, layer, x, router, bias, experts, ptrs, sh1, sh3, sh2, bias_vl, mask)
 
 
 def x_gpu(w: Workload, layer: int, out: torch.Tensor) -> None:

@@ -30,7 +30,7 @@ def assert_close(got, ref, what=""):
 def lib_cfg(w: W.Workload, max_tokens=None, path=0, timeout_us=0):
     import quantized_mixture_experts_router_gb300 as Q
     return Q.make_cfg(w.dim, w.inter, w.n_routed, w.topk, w.gate_temp, w.norm_topk_prob, w.route_scale,
-                      w.swiglu_limit, max_tokens or w.m, path, timeout_us)
+                      w.swiglu_limit, max_tokens or w.m, path, timeout_us, w.score_func)
 
 
 def gpu_forward(dl, path=0, m=None, ws=None, cfg=None):
@@ -47,8 +47,12 @@ def gpu_forward(dl, path=0, m=None, ws=None, cfg=None):
     tw = torch.empty((m, w.topk), dtype=torch.float32, device="cuda")
     ti = torch.empty((m, w.topk), dtype=torch.int32, device="cuda")
     lg = torch.empty((m, w.n_routed), dtype=torch.float32, device="cuda")
-    Q.moe_v41_forward(cfg, dl.x, m, dl.router_w, dl.bias, dl.expert_ptrs, w.shared_kind, dl.sh1, dl.sh3, dl.sh2,
-                      out, tw, ti, lg, ws)
+    if dl.image_mask is None:
+        Q.moe_v41_forward(cfg, dl.x, m, dl.router_w, dl.bias, dl.expert_ptrs, w.shared_kind, dl.sh1, dl.sh3, dl.sh2,
+                          out, tw, ti, lg, ws)
+    else:
+        Q.moe_v41_forward_vl(cfg, dl.x, m, dl.router_w, dl.bias, dl.bias_vl, dl.image_mask, dl.expert_ptrs,
+                             w.shared_kind, dl.sh1, dl.sh3, dl.sh2, out, tw, ti, lg, ws)
     status = Q.moe_v41_read_status(ws, clear=True)
     return dict(out=out.cpu().numpy(), topk_w=tw.cpu().numpy(), topk_idx=ti.cpu().numpy(),
                 logits=lg.cpu().numpy(), status=status, ws=ws)
@@ -65,5 +69,7 @@ def oracle_for(w: W.Workload, layer: int, given_logits=None, tokens=None, picked
     for e in need:
         experts[e] = W.expert_blocks(w, layer, e)
     sh = W.shared_weights(w, layer)
+    im = W.image_mask(w, layer)
+    bv = None if im is None else W.bias_vl_f32(w, layer)
     return oracle.moe_layer(oracle.cfg_of(w), x, R, b, experts, w.shared_kind, *sh, tokens=tokens,
-                            given_logits=given_logits)
+                            given_logits=given_logits, bias_vl=bv, image_mask=im)

@@ -31,7 +31,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _declared()
-    for n in ("moe_v41_route", "moe_v41_forward", "moe_v41_workspace_bytes", "moe_v41_read_status"):
+    for n in ("moe_v41_route", "moe_v41_forward", "moe_v41_workspace_bytes", "moe_v41_read_status",
+              "moe_v41_forward_vl", "moe_v41_route_vl", "moe_v41_select_from_logits_vl"):
         assert n in names
 
 
@@ -49,6 +50,10 @@ def test_workspace_sizing_is_host_only(lib):
     assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 17)) == 0     # topk above 16
     assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 4, 6)) == 0        # topk above n_routed
     assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, gate_temp=0.0)) == 0
+    for sf in (Q.MOE_SCORE_SIGMOID, Q.MOE_SCORE_SOFTMAX):                     # the Gate's other score functions
+        assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, max_tokens=8, score_func=sf)) == n
+    assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, score_func=3)) == 0
+    assert Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, score_func=-1)) == 0
     assert Q.strerror(Q.MOE_ERR_WORKSPACE).startswith("workspace")
 
 

@@ -110,6 +110,67 @@ def test_selection_nan_key_sets_status():
     assert nan == 1 and status & Q.MOE_STATUS_NAN_KEY
 
 
+def _select_gpu_vl(w, logits, bias, bias_vl, mask):
+    cfg = lib_cfg(w, max_tokens=logits.shape[0])
+    ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    Q.moe_v41_workspace_init(ws)
+    m = logits.shape[0]
+    tw = torch.empty((m, w.topk), dtype=torch.float32, device="cuda")
+    ti = torch.empty((m, w.topk), dtype=torch.int32, device="cuda")
+    Q.moe_v41_select_from_logits_vl(cfg, torch.from_numpy(logits).cuda(), m, torch.from_numpy(bias).cuda(),
+                                    torch.from_numpy(bias_vl).cuda(), torch.from_numpy(mask).cuda(), tw, ti, ws)
+    status = Q.moe_v41_read_status(ws, clear=True)
+    return tw.cpu().numpy(), ti.cpu().numpy(), status
+
+
+def _near_tie_logits(w, bias, c=0.5):
+    """logits whose sigmoid keys s + bias all land within a few f32 ulps of c,
+    so that the fast keys cannot separate the picks and the exact re-scoring
+    decides (ties between equal exact keys go to the lower id)"""
+    s = np.clip(c - bias.astype(np.float64), 1e-6, 1 - 1e-6)
+    return (w.gate_temp * np.log(s / (1.0 - s))).astype(np.float32)
+
+
+@pytest.mark.parametrize("sf", [1, 2])
+@pytest.mark.parametrize("name", ["decode_m1_40layer", "tiny"])
+def test_selection_score_funcs_bitexact(sf, name):
+    """Sigmoid and softmax scores (DeepSeek V4.1 model.py Gate.forward) with
+    image tokens picking on bias_vl: indices bit-exact, weights within f32
+    rounding of the oracle's."""
+    w = W.WORKLOADS[name].with_(score_func=sf)
+    rng = np.random.default_rng(23 + sf)
+    m = 200
+    logits = (rng.standard_normal((m, w.n_routed)) * 2).astype(np.float32)
+    bias = W.bias_f32(w.with_(m=1), 0)
+    bias_vl = W.bias_vl_f32(w.with_(m=1), 0)
+    logits[0] = 25.0                                  # equal logits
+    logits[1, ::3] = 40.0                             # saturated sigmoid / dominant softmax terms
+    logits[2, :5] = -200.0                            # exp underflow
+    logits[3] = _near_tie_logits(w, bias)             # near-ties on the token's keys
+    logits[4] = _near_tie_logits(w, bias_vl)          # the same for an image token
+    mask = (np.arange(m) % 3 == 1).astype(np.uint8)
+    mask[3], mask[4] = 0, 1
+    for b, bv in ((bias, bias_vl), (np.zeros_like(bias), np.full_like(bias, 0.01))):
+        tw, ti, status = _select_gpu_vl(w, logits, b, bv, mask)
+        rw, ri, nan = oracle.route_from_logits(oracle.cfg_of(w), logits, b, bv, mask)
+        np.testing.assert_array_equal(ti, ri)
+        np.testing.assert_allclose(tw, rw, rtol=2e-6, atol=0)
+        assert status == 0 and nan == 0
+
+
+def test_selection_softmax_nan_logit_makes_every_score_nan():
+    w = W.WORKLOADS["tiny"].with_(score_func=2)
+    logits = np.tile(np.arange(w.n_routed, dtype=np.float32), (2, 1))
+    logits[1, 5] = np.nan
+    bias = np.zeros(w.n_routed, np.float32)
+    tw, ti, status = _select_gpu_vl(w, logits, bias, bias, np.zeros(2, np.uint8))
+    rw, ri, nan = oracle.route_from_logits(oracle.cfg_of(w), logits, bias)
+    np.testing.assert_array_equal(ti, ri)
+    assert list(ti[1]) == list(range(w.topk)) and np.all(np.isnan(tw[1])) and np.all(np.isnan(rw[1]))
+    np.testing.assert_allclose(tw[0], rw[0], rtol=2e-6)
+    assert nan == w.n_routed and status & Q.MOE_STATUS_NAN_KEY
+
+
 # ----------------------------------------------------------------- layers
 
 def _check_layer(w, layer, res, tokens=None, picked_experts=True):
@@ -127,7 +188,11 @@ def _check_layer(w, layer, res, tokens=None, picked_experts=True):
                               W.router_bf16(w, layer))
     np.testing.assert_allclose(lg[sel], zr, rtol=1e-4, atol=1e-4)
     # picks from the oracle's own logits: expected identical
-    rw, ri, _ = oracle.route_from_logits(oracle.cfg_of(w), zr, W.bias_f32(w, layer))
+    im = W.image_mask(w, layer)
+    bv = None if im is None else W.bias_vl_f32(w, layer)
+    if im is not None and tokens is not None:
+        im = im[sel]
+    rw, ri, _ = oracle.route_from_logits(oracle.cfg_of(w), zr, W.bias_f32(w, layer), bv, im)
     flips = int(np.sum(np.any(np.sort(ri, 1) != np.sort(r.topk_idx, 1), axis=1)))
     return l2, mx, flips
 
@@ -152,6 +217,22 @@ def test_tiny_decode_variants(variant):
     res = gpu_forward(dl, path=Q.MOE_PATH_DECODE)
     assert res["status"] == 0
     _check_layer(w, 0, res)
+
+
+@pytest.mark.parametrize("sf,vl,n_routed", [(1, False, 16), (2, False, 16), (0, True, 16), (0, True, 384),
+                                             (1, True, 384), (2, True, 384)])
+@pytest.mark.parametrize("m", [1, 8])
+def test_tiny_decode_score_funcs_and_image_tokens(sf, vl, n_routed, m):
+    """The Gate's score functions and the image-token bias through the fused
+    decode kernel (384 experts: the register-resident selection path)."""
+    w = W.WORKLOADS["tiny"].with_(m=m, score_func=sf, n_routed=n_routed, topk=2 if n_routed == 16 else 6,
+                                  image_frac=(1.0 if m == 1 else 0.5) if vl else 0.0)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    assert (dl.image_mask is not None) == vl
+    res = gpu_forward(dl, path=Q.MOE_PATH_DECODE)
+    assert res["status"] == 0
+    _, _, flips = _check_layer(w, 0, res)
+    assert flips == 0
 
 
 def test_tiny_decode_outliers_clip():

@@ -142,6 +142,43 @@ def test_route_above_eight_tokens():
     np.testing.assert_allclose(tw.cpu().numpy(), rw, rtol=2e-6)
 
 
+@pytest.mark.parametrize("sf,vl,n_routed,m", [(1, False, 16, 100), (2, False, 16, 100), (0, True, 16, 100),
+                                               (1, True, 384, 64), (2, True, 384, 64)])
+def test_tiny_prefill_score_funcs_and_image_tokens(sf, vl, n_routed, m):
+    """The Gate's sigmoid and softmax scores and the image-token bias through
+    the prefill kernels."""
+    w = W.WORKLOADS["tiny"].with_(m=m, score_func=sf, n_routed=n_routed, topk=2 if n_routed == 16 else 6,
+                                  image_frac=0.4 if vl else 0.0)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    res = gpu_forward(dl, path=Q.MOE_PATH_PREFILL)
+    assert res["status"] == 0
+    _check(w, 0, res)
+
+
+@pytest.mark.parametrize("m,path", [(5, Q.MOE_PATH_AUTO), (77, Q.MOE_PATH_AUTO)])
+def test_route_vl_softmax(m, path):
+    """moe_v41_route_vl on both router paths (decode kernel for m <= 8,
+    tensor-core GEMM plus selection above): softmax scores, image tokens."""
+    w = W.WORKLOADS["tiny"].with_(m=m, score_func=2, image_frac=0.5)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    cfg = lib_cfg(w, path=path)
+    ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    Q.moe_v41_workspace_init(ws)
+    lg = torch.empty((w.m, w.n_routed), dtype=torch.float32, device="cuda")
+    tw = torch.empty((w.m, w.topk), dtype=torch.float32, device="cuda")
+    ti = torch.empty((w.m, w.topk), dtype=torch.int32, device="cuda")
+    Q.moe_v41_route_vl(cfg, dl.x, w.m, dl.router_w, dl.bias, dl.bias_vl, dl.image_mask, lg, tw, ti, ws)
+    assert Q.moe_v41_read_status(ws, clear=True) == 0
+    logits = lg.cpu().numpy()
+    rw, ri, _ = oracle.route_from_logits(oracle.cfg_of(w), logits, W.bias_f32(w, 0), W.bias_vl_f32(w, 0),
+                                         W.image_mask(w, 0))
+    np.testing.assert_array_equal(ti.cpu().numpy(), ri)
+    np.testing.assert_allclose(tw.cpu().numpy(), rw, rtol=2e-6)
+    # the image tokens really picked on bias_vl: their picks under the text bias differ somewhere
+    _, ri_text, _ = oracle.route_from_logits(oracle.cfg_of(w), logits, W.bias_f32(w, 0))
+    assert np.any(ri_text != ri)
+
+
 # ------------------------------------------------------ full-size prefill
 
 def _sample_tokens(w, res, n, must=()):
