@@ -57,6 +57,11 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=30)
     ap.add_argument("--prefill-m", type=int, default=0, help="tokens of the prefill call (default: the workload's)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-streamed", action="store_true")
+    ap.add_argument("--streamed-layers", type=int, default=4, help="layers of the host arena (streamed leg)")
+    ap.add_argument("--streamed-slots", type=int, default=256, help="HBM expert slots of the streamed leg")
+    ap.add_argument("--streamed-tokens", type=int, default=64, help="timed tokens of the streamed leg")
+    ap.add_argument("--prefetch-k", type=int, default=6, help="predicted next-layer experts fetched ahead")
     ap.add_argument("--graph", type=int, default=1,
                     help="1: time the decode step as one CUDA-graph replay of its layer calls; 0: eager launches")
     return ap.parse_args()
@@ -470,6 +475,115 @@ def run_prefill(args, local_rank):
                 clocks=clk, e2e=e2e, launches_per_call=launches)
 
 
+def _mem_available() -> int:
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def run_streamed(args, local_rank):
+    """The decode workload with the routed experts streamed: every expert of
+    a few layers in a page-locked host arena, a least-recently-used set of HBM
+    slots, one token at a time through the layers with moe_v41_forward_streamed
+    (route, host span, fetch, forward), once without and once with the next
+    layer's experts predicted and fetched ahead.  Each token's layers take the
+    same x (a stand-in for the residual stream's layer-to-layer correlation),
+    so a prediction of prefetch_k = topk is the next layer's true routing."""
+    import torch
+    import quantized_mixture_experts_router_gb300 as Q
+    from synth.device import fill_experts_gpu, slot_layout, stage_layer
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.empty_cache()
+    w = W.WORKLOADS[args.workload]
+    o1, o3, o2, slot = slot_layout(w)
+    layer_bytes = w.n_routed * slot
+    Ls = args.streamed_layers
+    avail = _mem_available()
+    while Ls > 1 and Ls * layer_bytes * 3 > avail:
+        Ls -= 1
+    if Ls * layer_bytes * 3 > avail:
+        return {"skipped": f"host memory: {avail / 1e9:.0f} GB available, one layer's arena is {layer_bytes / 1e9:.1f} GB"}
+    S = args.streamed_slots
+    free, _ = torch.cuda.mem_get_info()
+    if S * slot + layer_bytes + Ls * 100e6 > free - (4 << 30):
+        S = max(2 * w.topk, int((free - (4 << 30) - layer_bytes - Ls * 100e6) // slot))
+    cudart = torch.cuda.cudart()
+    arena = torch.empty((Ls, w.n_routed, slot), dtype=torch.uint8)
+    rc = cudart.cudaHostRegister(arena.data_ptr(), arena.numel(), 0)
+    if int(rc) != 0:
+        return {"skipped": f"cudaHostRegister of the {arena.numel() / 1e9:.1f} GB arena failed ({int(rc)})"}
+    try:
+        stagebuf = torch.empty((w.n_routed, slot), dtype=torch.uint8, device=dev)
+        for l in range(Ls):
+            fill_experts_gpu(w, l, stagebuf)
+            arena[l].copy_(stagebuf)
+        del stagebuf
+        layers = [stage_layer(w, l, device=dev, experts_on_gpu=True, bulk_on_gpu=True, slots=1) for l in range(Ls)]
+        xs = [stage_x(w.with_(seed=w.seed + 7000 + t), 0, dev) for t in range(16)]
+        cfg = Q.make_cfg(w.dim, w.inter, w.n_routed, w.topk, w.gate_temp, w.norm_topk_prob, w.route_scale,
+                         w.swiglu_limit, max_tokens=w.m)
+        ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+        Q.moe_v41_workspace_init(ws)
+        out = torch.empty((w.m, w.dim), dtype=torch.float32, device=dev)
+        tw = torch.empty((w.m, w.topk), dtype=torch.float32, device=dev)
+        ti = torch.empty((w.m, w.topk), dtype=torch.int32, device=dev)
+        stream = torch.cuda.current_stream()
+        copy_stream = torch.cuda.Stream(device=dev)
+        runs = []
+        for P in ([0, args.prefetch_k] if args.prefetch_k > 0 else [0]):
+            slots = torch.empty((S, slot), dtype=torch.uint8, device=dev)
+            tables = torch.empty((Ls, w.n_routed, 3), dtype=torch.int64, device=dev)
+            cache = Q.ExpertCache(Ls, w.n_routed, S, slot, o1, o3, o2, arena, slots, tables)
+            host = torch.empty(w.m * w.topk + P, dtype=torch.int32, pin_memory=True)
+
+            def token(t):
+                x = xs[t % len(xs)]
+                for l in range(Ls):
+                    d = layers[l]
+                    n = layers[l + 1] if l + 1 < Ls else None
+                    Q.moe_v41_forward_streamed(cfg, cache, l, x, w.m, d.router_w, d.bias,
+                                               None if n is None else n.router_w, None if n is None else n.bias, P,
+                                               w.shared_kind, d.sh1, d.sh3, d.sh2, out, tw, ti, ws, host, stream,
+                                               copy_stream)
+            Tw = max(args.warmup, S // (w.topk * Ls) + 4)
+            for t in range(Tw):
+                token(t)
+            torch.cuda.synchronize()
+            st0 = cache.stats()
+            T = args.streamed_tokens
+            t0 = time.perf_counter()
+            for t in range(Tw, Tw + T):
+                token(t)
+            torch.cuda.synchronize()
+            sec = time.perf_counter() - t0
+            st1 = cache.stats()
+            status = Q.moe_v41_read_status(ws, stream, clear=True)
+            if status:
+                raise RuntimeError(f"device status {status} in the streamed leg")
+            dd = {k: st1[k] - st0[k] for k in st1}
+            calls = T * Ls
+            runs.append({"prefetch_k": P, "ms_per_layer_call": 1000.0 * sec / calls, "tokens_per_s": T / sec,
+                         "tokens_per_s_40_layers": T / sec * Ls / 40.0,
+                         "hit_rate": dd["hits"] / max(1, dd["hits"] + dd["misses"]),
+                         "prefetch_hits_per_call": dd["prefetch_hits"] / calls,
+                         "misses_per_call": dd["misses"] / calls, "bytes_copied_per_call": dd["bytes_copied"] / calls,
+                         "copy_gbs": dd["bytes_copied"] / sec / 1e9})
+            cache.close()
+            del slots, tables, cache
+        return {"workload": w.name + " (experts streamed)", "arena_layers": Ls, "arena_bytes": arena.numel(),
+                "slots": S, "slot_bytes": slot, "hbm_slot_bytes": S * slot, "timed_tokens": args.streamed_tokens,
+                "layers_per_token": Ls, "timing": "wall clock over the timed tokens, both streams drained at the ends",
+                "x": "one seeded x per token, the same for every layer of the token", "runs": runs}
+    finally:
+        torch.cuda.synchronize()
+        cudart.cudaHostUnregister(arena.data_ptr())
+
+
 def stage_x(w, l, dev):
     import torch
     from synth.device import x_gpu
@@ -509,6 +623,7 @@ def main():
         dist.init_process_group("nccl")
     r = run_ours(args, rank, world, local_rank)
     pf = None if args.no_prefill else run_prefill(args, local_rank)
+    sm = None if (args.no_streamed or world > 1) else run_streamed(args, local_rank)
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -557,6 +672,8 @@ def main():
             p["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
                                  "sample": desc + f", {dt:.1f} s"}
         line["prefill"] = p
+    if sm:
+        line["streamed"] = sm
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -33,6 +33,19 @@ class moe_v41_cfg(ctypes.Structure):
                 ("path", ctypes.c_int32), ("wait_timeout_us", ctypes.c_uint32), ("score_func", ctypes.c_int32)]
 
 
+class moe_v41_cache_cfg(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_routed", ctypes.c_int32), ("n_slots", ctypes.c_int32),
+                ("slot_bytes", ctypes.c_uint64), ("off_w1", ctypes.c_uint64), ("off_w3", ctypes.c_uint64),
+                ("off_w2", ctypes.c_uint64), ("arena", ctypes.c_void_p), ("slots", ctypes.c_void_p),
+                ("tables", ctypes.c_void_p)]
+
+
+class moe_v41_cache_stats(ctypes.Structure):
+    _fields_ = [("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64), ("evictions", ctypes.c_uint64),
+                ("bytes_copied", ctypes.c_uint64), ("prefetched", ctypes.c_uint64),
+                ("prefetch_hits", ctypes.c_uint64)]
+
+
 _lib = None
 
 
@@ -60,9 +73,21 @@ def lib():
         L.moe_v41_kernel_launches.restype = i32
         L.moe_v41_strerror.restype = ctypes.c_char_p
         L.moe_v41_strerror.argtypes = [i32]
+        cp = ctypes.c_void_p
+        L.moe_v41_cache_create.argtypes = [ctypes.POINTER(moe_v41_cache_cfg), vp, ctypes.POINTER(cp)]
+        L.moe_v41_cache_destroy.argtypes = [cp]
+        L.moe_v41_cache_fetch.argtypes = [cp, i32, vp, i32, i32, vp]
+        L.moe_v41_cache_wait.argtypes = [cp, i32, vp]
+        L.moe_v41_cache_reads.argtypes = [cp, i32, vp, i32, vp]
+        L.moe_v41_cache_slot_of.argtypes = [cp, i32, i32]
+        L.moe_v41_cache_get_stats.argtypes = [cp, ctypes.POINTER(moe_v41_cache_stats)]
+        L.moe_v41_forward_streamed.argtypes = [cfgp, cp, i32, vp, i32, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp,
+                                               vp, vp, sz, vp, vp, vp]
         for f in ("moe_v41_workspace_init", "moe_v41_quantize_q8_1", "moe_v41_select_from_logits", "moe_v41_route",
                   "moe_v41_forward", "moe_v41_read_status", "moe_v41_forward_noalloc",
-                  "moe_v41_select_from_logits_vl", "moe_v41_route_vl", "moe_v41_forward_vl"):
+                  "moe_v41_select_from_logits_vl", "moe_v41_route_vl", "moe_v41_forward_vl", "moe_v41_cache_create",
+                  "moe_v41_cache_destroy", "moe_v41_cache_fetch", "moe_v41_cache_wait", "moe_v41_cache_reads",
+                  "moe_v41_cache_slot_of", "moe_v41_cache_get_stats", "moe_v41_forward_streamed"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -177,3 +202,81 @@ def moe_v41_read_status(ws, stream=None, clear: bool = False) -> int:
     v = ctypes.c_uint32(0)
     _check(lib().moe_v41_read_status(_p(ws), _s(stream), ctypes.byref(v), int(clear)), "moe_v41_read_status")
     return v.value
+
+
+# ------------------------------------------------------------ expert cache
+
+def _ids(experts):
+    a = [int(e) for e in experts]
+    return (ctypes.c_int32 * max(1, len(a)))(*a), len(a)
+
+
+class ExpertCache:
+    """include/moe_v41_cache.h: routed experts of a host arena held in a
+    least-recently-used set of HBM slots, with the per-layer slot pointer
+    tables moe_v41_forward reads.  arena: page-locked host tensor (or address)
+    of [n_layers, n_routed, slot_bytes]; slots: device [n_slots, slot_bytes];
+    tables: device int64 [n_layers, n_routed, 3].  With slots and tables None
+    the cache only simulates the replacement policy (no CUDA call)."""
+
+    def __init__(self, n_layers, n_routed, n_slots, slot_bytes, off_w1, off_w3, off_w2, arena=None, slots=None,
+                 tables=None, stream=None):
+        self.sim = slots is None and tables is None
+        self.cfg = moe_v41_cache_cfg(n_layers, n_routed, n_slots, slot_bytes, off_w1, off_w3, off_w2, _p(arena),
+                                     _p(slots), _p(tables))
+        self._keep = (arena, slots, tables)
+        self._h = ctypes.c_void_p()
+        _check(lib().moe_v41_cache_create(ctypes.byref(self.cfg), None if self.sim else _s(stream),
+                                          ctypes.byref(self._h)), "moe_v41_cache_create")
+        self.tables = tables
+
+    def _st(self, stream):
+        return None if self.sim else _s(stream)
+
+    def fetch(self, layer, experts, prefetch=False, copy_stream=None):
+        a, n = _ids(experts)
+        _check(lib().moe_v41_cache_fetch(self._h, layer, a, n, int(bool(prefetch)), self._st(copy_stream)),
+               "moe_v41_cache_fetch")
+
+    def wait(self, layer, stream=None):
+        _check(lib().moe_v41_cache_wait(self._h, layer, self._st(stream)), "moe_v41_cache_wait")
+
+    def reads(self, layer, experts=None, stream=None):
+        if experts is None:
+            _check(lib().moe_v41_cache_reads(self._h, layer, None, 0, self._st(stream)), "moe_v41_cache_reads")
+        else:
+            a, n = _ids(experts)
+            _check(lib().moe_v41_cache_reads(self._h, layer, a, n, self._st(stream)), "moe_v41_cache_reads")
+
+    def slot_of(self, layer, expert) -> int:
+        return int(lib().moe_v41_cache_slot_of(self._h, layer, expert))
+
+    def stats(self) -> dict:
+        st = moe_v41_cache_stats()
+        _check(lib().moe_v41_cache_get_stats(self._h, ctypes.byref(st)), "moe_v41_cache_get_stats")
+        return {f: int(getattr(st, f)) for f, _ in moe_v41_cache_stats._fields_}
+
+    def table(self, layer):
+        """the device slot pointer table of one layer ([n_routed, 3] int64 view)"""
+        return self.tables[layer]
+
+    def close(self):
+        if self._h:
+            lib().moe_v41_cache_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def moe_v41_forward_streamed(cfg, cache: ExpertCache, layer, x, m, router_w, bias, next_router_w, next_bias,
+                             prefetch_k, shared_kind, sh_w1, sh_w3, sh_w2, out, topk_w, topk_idx, ws, host_picks,
+                             stream=None, copy_stream=None):
+    _check(lib().moe_v41_forward_streamed(ctypes.byref(cfg), cache._h, layer, _p(x), m, _p(router_w), _p(bias),
+                                          _p(next_router_w), _p(next_bias), prefetch_k, shared_kind, _p(sh_w1),
+                                          _p(sh_w3), _p(sh_w2), _p(out), _p(topk_w), _p(topk_idx), _p(ws),
+                                          _nbytes(ws), _p(host_picks), _s(stream), _s(copy_stream)),
+           "moe_v41_forward_streamed")

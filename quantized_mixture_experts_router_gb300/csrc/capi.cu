@@ -92,6 +92,30 @@ PrefillParams prefill_params(const moe_v41_cfg* c, const void* x, int m, const v
 
 }  // namespace
 
+int moe::route_topk(const moe_v41_cfg* cfg, int k, const void* x, int m, const void* router_w, const float* bias,
+                    int32_t** idx_out, void* ws, size_t ws_bytes, cudaStream_t s) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!x || !router_w || !bias || !idx_out || m < 1 || m > cfg->max_tokens || m > DECODE_MAX_M) return MOE_ERR_ARG;
+  if (k < 1 || k > MAX_TOPK || k > cfg->n_routed) return MOE_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(router_w, 16)) return MOE_ERR_ALIGN;
+  if ((rc = check_ws(cfg, ws, ws_bytes))) return rc;
+  const WsLayout L = ws_layout(*cfg);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* idx = reinterpret_cast<int32_t*>(w + L.pred);
+  float* wt = reinterpret_cast<float*>(idx + (size_t)m * k);
+  *idx_out = idx;
+  if (cfg->path != MOE_PATH_PREFILL) {
+    RouteParams p = route_params(cfg, x, m, router_w, bias, nullptr, nullptr, nullptr, wt, idx, w, L);
+    p.k = k;
+    return launch_route_decode(p, s);
+  }
+  PrefillParams p = prefill_params(cfg, x, m, router_w, bias, nullptr, nullptr, nullptr, MOE_SHARED_BF16, nullptr,
+                                   nullptr, nullptr, nullptr, wt, idx, nullptr, w, L);
+  p.k = k;
+  return launch_prefill_route(p, s);
+}
+
 extern "C" {
 
 size_t moe_v41_workspace_bytes(const moe_v41_cfg* cfg) {

@@ -70,7 +70,7 @@ struct PrefillLayout {
 
 // Byte offsets of the workspace regions (all 256-B aligned).
 struct WsLayout {
-  size_t ctrl, plan, logits, sk, xq8, xu, hu, shh, pre, total;
+  size_t ctrl, plan, logits, sk, xq8, xu, hu, shh, pred, pre, total;
   PrefillLayout P;
 };
 
@@ -128,6 +128,7 @@ inline WsLayout ws_layout(const moe_v41_cfg& c) {
   L.xu = take(Td * unit_bytes(c.dim));
   L.hu = take(vecs * unit_bytes(c.inter));
   L.shh = take(Td * c.inter * 2);
+  L.pred = take(Td * MAX_TOPK * 8);  // predicted picks of the next layer (weights, ids)
   if (prefill_possible(c)) {
     L.P = prefill_layout(c);
     L.pre = take(L.P.total);

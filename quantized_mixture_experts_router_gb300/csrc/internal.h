@@ -97,4 +97,11 @@ int launch_prefill_route(const PrefillParams& p, cudaStream_t s);
 int prefill_launches(int shared_kind);
 size_t decode_smem_bytes();
 
+// The routing of m tokens with k picks per token (k may differ from
+// cfg->topk; 1 <= k <= min(MAX_TOPK, n_routed)) into the workspace's pred
+// region: *idx_out receives its device address ([m, k] int32, the weights
+// follow the ids).  The router kernel and order are those of moe_v41_route.
+int route_topk(const moe_v41_cfg* cfg, int k, const void* x, int m, const void* router_w, const float* bias,
+               int32_t** idx_out, void* ws, size_t ws_bytes, cudaStream_t s);
+
 }  // namespace moe

@@ -39,6 +39,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "bf16dot.cuh"
 #include "select.cuh"
 
 namespace moe {
@@ -178,33 +179,6 @@ __device__ __forceinline__ Item decode_ticket(int stream, unsigned t, const Size
   }
 }
 
-// ---------------------------------------------------------- warp helpers
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// c + a*b for the low (hi = 0) or high bf16 halves of a and b, with one f32
-// rounding: the mixed-precision fma takes the bf16 operands directly, the same
-// result as fmaf on the widened values without the two unpacking instructions.
-__device__ __forceinline__ float fma_bf16(uint32_t a, uint32_t b, float c, int hi) {
-  unsigned short al, ah, bl, bh;
-  asm("mov.b32 {%0, %1}, %2;" : "=h"(al), "=h"(ah) : "r"(a));
-  asm("mov.b32 {%0, %1}, %2;" : "=h"(bl), "=h"(bh) : "r"(b));
-  if (hi) asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(c) : "h"(ah), "h"(bh));
-  else asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(c) : "h"(al), "h"(bl));
-  return c;
-}
-
-// 8 bf16 products into two accumulators (two independent FMA chains)
-__device__ __forceinline__ void dot8(float2& acc, const uint4& w, const uint4& x) {
-  acc.x = fma_bf16(w.x, x.x, acc.x, 0); acc.y = fma_bf16(w.x, x.x, acc.y, 1);
-  acc.x = fma_bf16(w.y, x.y, acc.x, 0); acc.y = fma_bf16(w.y, x.y, acc.y, 1);
-  acc.x = fma_bf16(w.z, x.z, acc.x, 0); acc.y = fma_bf16(w.z, x.z, acc.y, 1);
-  acc.x = fma_bf16(w.w, x.w, acc.x, 0); acc.y = fma_bf16(w.w, x.w, acc.y, 1);
-}
-
 // 16 bytes of an activation vector: from the block's shared-memory copy (S,
 // byte offset so + off), else from global memory through L2 (the vector may
 // have been written by other blocks of this kernel)
@@ -252,7 +226,7 @@ __device__ __noinline__ float4 bf16_rows_dot(uint32_t w, uint32_t rs, uint32_t v
   }
   float o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int r = 0; r < R; ++r) o[r] = warp_sum((a[r].x + a[r].y) + (b[r].x + b[r].y));
+  for (int r = 0; r < R; ++r) o[r] = warp_sum(lane_total(a[r], b[r]));
   return make_float4(o[0], o[1], o[2], o[3]);
 }
 

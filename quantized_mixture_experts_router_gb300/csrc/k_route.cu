@@ -10,6 +10,7 @@
 // DeepSeek V4.1 atlas "Mixture of experts", model.py Gate.forward (sigmoid
 // and softmax scores; bias_vl for image tokens).
 #include "internal.h"
+#include "bf16dot.cuh"
 #include "select.cuh"
 
 namespace moe {
@@ -49,43 +50,29 @@ __global__ void __launch_bounds__(256) k_route_decode(RouteParams p) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int chunks = p.D / 8;  // 16-B chunks of a bf16 row
   if (gw < p.N) {
+    // the fused decode kernel's order (bf16dot.cuh): same logits, bit for bit
     const uint4* wrow = reinterpret_cast<const uint4*>(p.router_w + (size_t)gw * p.D);
-    float acc[DECODE_MAX_M];
+    float2 a[DECODE_MAX_M], b[DECODE_MAX_M];
 #pragma unroll
-    for (int t = 0; t < DECODE_MAX_M; ++t) acc[t] = 0.f;
-    for (int c0 = 0; c0 < chunks; c0 += 32 * 8) {
-      uint4 wv[8];
+    for (int t = 0; t < DECODE_MAX_M; ++t) a[t] = b[t] = make_float2(0.f, 0.f);
+#pragma unroll 1
+    for (int ch = lane; ch < chunks; ch += 64) {
+      const bool two = ch + 32 < chunks;
+      const uint4 w0 = __ldg(wrow + ch);
+      const uint4 w1 = two ? __ldg(wrow + ch + 32) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int c = c0 + lane + 32 * i;
-        wv[i] = c < chunks ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int c = c0 + lane + 32 * i;
-        if (c >= chunks) break;
-        const float w0 = bf16lo(wv[i].x), w1 = bf16hi(wv[i].x), w2 = bf16lo(wv[i].y), w3 = bf16hi(wv[i].y);
-        const float w4 = bf16lo(wv[i].z), w5 = bf16hi(wv[i].z), w6 = bf16lo(wv[i].w), w7 = bf16hi(wv[i].w);
-#pragma unroll
-        for (int t = 0; t < DECODE_MAX_M; ++t) {
-          if (t < p.m) {
-            const uint4 xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.D) + c);
-            float a = acc[t];
-            a = fmaf(w0, bf16lo(xv.x), a); a = fmaf(w1, bf16hi(xv.x), a);
-            a = fmaf(w2, bf16lo(xv.y), a); a = fmaf(w3, bf16hi(xv.y), a);
-            a = fmaf(w4, bf16lo(xv.z), a); a = fmaf(w5, bf16hi(xv.z), a);
-            a = fmaf(w6, bf16lo(xv.w), a); a = fmaf(w7, bf16hi(xv.w), a);
-            acc[t] = a;
-          }
+      for (int t = 0; t < DECODE_MAX_M; ++t) {
+        if (t < p.m) {
+          const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.D);
+          dot8(a[t], w0, __ldg(xr + ch));
+          if (two) dot8(b[t], w1, __ldg(xr + ch + 32));
         }
       }
     }
 #pragma unroll
     for (int t = 0; t < DECODE_MAX_M; ++t) {
-      float a = acc[t];
-#pragma unroll
-      for (int o = 16; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      if (lane == 0 && t < p.m) p.logits[(size_t)t * p.N + gw] = a;
+      const float z = warp_sum(lane_total(a[t], b[t]));
+      if (lane == 0 && t < p.m) p.logits[(size_t)t * p.N + gw] = z;
     }
   } else {
     // q8_1 of x: one warp per q8_1 block
