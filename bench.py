@@ -522,7 +522,17 @@ def run_streamed(args, local_rank):
         for l in range(Ls):
             fill_experts_gpu(w, l, stagebuf)
             arena[l].copy_(stagebuf)
-        del stagebuf
+        # the link's own rate: plain arena -> HBM copies of whole expert slots
+        nprobe = min(16, w.n_routed)
+        probe = stagebuf[:nprobe]
+        probe.copy_(arena[0, :nprobe], non_blocking=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(3):
+            probe.copy_(arena[0, :nprobe], non_blocking=True)
+        torch.cuda.synchronize()
+        link_gbs = 3 * nprobe * slot / (time.perf_counter() - t0) / 1e9
+        del stagebuf, probe
         layers = [stage_layer(w, l, device=dev, experts_on_gpu=True, bulk_on_gpu=True, slots=1) for l in range(Ls)]
         xs = [stage_x(w.with_(seed=w.seed + 7000 + t), 0, dev) for t in range(16)]
         cfg = Q.make_cfg(w.dim, w.inter, w.n_routed, w.topk, w.gate_temp, w.norm_topk_prob, w.route_scale,
@@ -572,12 +582,16 @@ def run_streamed(args, local_rank):
                          "hit_rate": dd["hits"] / max(1, dd["hits"] + dd["misses"]),
                          "prefetch_hits_per_call": dd["prefetch_hits"] / calls,
                          "misses_per_call": dd["misses"] / calls, "bytes_copied_per_call": dd["bytes_copied"] / calls,
-                         "copy_gbs": dd["bytes_copied"] / sec / 1e9})
+                         "copy_gbs": dd["bytes_copied"] / sec / 1e9,
+                         "link_bound_ms_per_call": dd["bytes_copied"] / calls / (link_gbs * 1e9) * 1e3,
+                         "frac_of_link": dd["bytes_copied"] / sec / 1e9 / link_gbs})
             cache.close()
             del slots, tables, cache
         return {"workload": w.name + " (experts streamed)", "arena_layers": Ls, "arena_bytes": arena.numel(),
                 "slots": S, "slot_bytes": slot, "hbm_slot_bytes": S * slot, "timed_tokens": args.streamed_tokens,
-                "layers_per_token": Ls, "timing": "wall clock over the timed tokens, both streams drained at the ends",
+                "layers_per_token": Ls, "link_gbs": link_gbs,
+                "link": "arena -> HBM rate of plain copies of whole expert slots, measured in this run",
+                "timing": "wall clock over the timed tokens, both streams drained at the ends",
                 "x": "one seeded x per token, the same for every layer of the token", "runs": runs}
     finally:
         torch.cuda.synchronize()

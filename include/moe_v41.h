@@ -67,8 +67,9 @@ typedef struct {
 enum { MOE_SCORE_SQRTSOFTPLUS = 0, MOE_SCORE_SIGMOID = 1, MOE_SCORE_SOFTMAX = 2 };
 
 enum {
-  MOE_PATH_AUTO = 0,    /* decode kernels for m <= 8, prefill kernels above */
-  MOE_PATH_DECODE = 1,  /* decode kernels for any m <= 8 (error above) */
+  MOE_PATH_AUTO = 0,    /* decode kernels for m <= 8 when dim <= 5120 and inter <= 3328 (the widths one
+                           decode stage holds), prefill kernels otherwise */
+  MOE_PATH_DECODE = 1,  /* decode kernels for any m <= 8 (error above, or at wider shapes) */
   MOE_PATH_PREFILL = 2  /* prefill kernels for any m */
 };
 
@@ -133,7 +134,9 @@ MOE_API int moe_v41_select_from_logits_vl(const moe_v41_cfg* cfg, const float* l
 /* Router logits and routing for m tokens (the metrale route call, with the
  * selection on the device): x bf16 [m, dim], router_w bf16 [n_routed, dim]
  * (16-B aligned), bias f32 [n_routed].  logits_out (may be NULL) receives the
- * f32 logits [m, n_routed]. */
+ * f32 logits [m, n_routed].  The router kernel is the one the forward of the
+ * same tokens runs, with the same accumulation order, so the logits and the
+ * picks equal the forward's bit for bit. */
 MOE_API int moe_v41_route(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w, const float* bias,
                   float* logits_out, float* topk_w, int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream);
 MOE_API int moe_v41_route_vl(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w, const float* bias,
@@ -142,8 +145,8 @@ MOE_API int moe_v41_route_vl(const moe_v41_cfg* cfg, const void* x, int m, const
 
 /* One MoE layer forward for m tokens (the metrale MoeV41::forward call, all
  * experts resident).  Up to eight tokens run the decode kernels (one
- * persistent launch of integer-dot GEMVs); above that, or with
- * MOE_PATH_PREFILL, the prefill kernels (tokens grouped by expert, tensor-core
+ * persistent launch of integer-dot GEMVs); above that, at widths the decode
+ * kernel does not take, or with MOE_PATH_PREFILL, the prefill kernels (tokens grouped by expert, tensor-core
  * GEMMs on dequantised tiles; router logits then carry the tensor cores' f32
  * accumulation order).
  *   x           bf16 [m, dim], 16-B aligned

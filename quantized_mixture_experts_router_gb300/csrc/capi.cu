@@ -43,7 +43,7 @@ uint64_t timeout_ns(const moe_v41_cfg* c) {
 bool use_decode(const moe_v41_cfg* c, int m) {
   if (c->path == MOE_PATH_DECODE) return true;
   if (c->path == MOE_PATH_PREFILL) return false;
-  return m <= DECODE_MAX_M;
+  return m <= DECODE_MAX_M && decode_fits(c->dim, c->inter);
 }
 
 RouteParams route_params(const moe_v41_cfg* c, const void* x, int m, const void* router_w, const float* bias,
@@ -105,7 +105,7 @@ int moe::route_topk(const moe_v41_cfg* cfg, int k, const void* x, int m, const v
   int32_t* idx = reinterpret_cast<int32_t*>(w + L.pred);
   float* wt = reinterpret_cast<float*>(idx + (size_t)m * k);
   *idx_out = idx;
-  if (cfg->path != MOE_PATH_PREFILL) {
+  if (use_decode(cfg, m)) {
     RouteParams p = route_params(cfg, x, m, router_w, bias, nullptr, nullptr, nullptr, wt, idx, w, L);
     p.k = k;
     return launch_route_decode(p, s);
@@ -174,7 +174,8 @@ int moe_v41_route_vl(const moe_v41_cfg* cfg, const void* x, int m, const void* r
   if ((rc = check_ws(cfg, ws, ws_bytes))) return rc;
   const WsLayout L = ws_layout(*cfg);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  if (m <= DECODE_MAX_M && cfg->path != MOE_PATH_PREFILL) {
+  // the router kernel of the forward that would take these tokens (same logits)
+  if (m <= DECODE_MAX_M && use_decode(cfg, m)) {
     RouteParams p = route_params(cfg, x, m, router_w, bias, bias_vl, image_mask, logits_out, topk_w, topk_idx, w, L);
     return launch_route_decode(p, (cudaStream_t)stream);
   }

@@ -108,9 +108,17 @@ inline PrefillLayout prefill_layout(const moe_v41_cfg& c) {
   return L;
 }
 
-// Whether a configuration can take the prefill kernels.
+// Whether the fused decode kernel's stages hold one task's rows at these
+// widths (defined with the kernel).
+bool decode_fits(int D, int I);
+
+// Whether a configuration can take the prefill kernels: always with
+// MOE_PATH_PREFILL; with MOE_PATH_AUTO when some call may have more than 8
+// tokens, or when the decode kernel cannot take these widths (then every call
+// runs the prefill kernels).
 inline bool prefill_possible(const moe_v41_cfg& c) {
-  return c.path == MOE_PATH_PREFILL || (c.path == MOE_PATH_AUTO && c.max_tokens > DECODE_MAX_M);
+  return c.path == MOE_PATH_PREFILL ||
+         (c.path == MOE_PATH_AUTO && (c.max_tokens > DECODE_MAX_M || !decode_fits(c.dim, c.inter)));
 }
 
 inline WsLayout ws_layout(const moe_v41_cfg& c) {

@@ -97,6 +97,15 @@ def test_selection_config_variants():
         rw, ri, _ = oracle.route_from_logits(oracle.cfg_of(w), logits, bias)
         np.testing.assert_array_equal(ti, ri)
         np.testing.assert_allclose(tw, rw, rtol=2e-6)
+    # the largest routing: 1024 experts, 16 picks
+    big = base.with_(n_routed=1024, topk=16)
+    logits = (rng.standard_normal((64, 1024)) * 3).astype(np.float32)
+    bias = W.bias_f32(big.with_(m=1), 0)
+    for w in (big, big.with_(score_func=1), big.with_(score_func=2)):
+        tw, ti, _ = _select_gpu(w, logits, bias)
+        rw, ri, _ = oracle.route_from_logits(oracle.cfg_of(w), logits, bias)
+        np.testing.assert_array_equal(ti, ri)
+        np.testing.assert_allclose(tw, rw, rtol=2e-6)
 
 
 def test_selection_nan_key_sets_status():
@@ -229,6 +238,18 @@ def test_tiny_decode_score_funcs_and_image_tokens(sf, vl, n_routed, m):
                                   image_frac=(1.0 if m == 1 else 0.5) if vl else 0.0)
     dl = stage_layer(w, 0, experts_on_gpu=False)
     assert (dl.image_mask is not None) == vl
+    res = gpu_forward(dl, path=Q.MOE_PATH_DECODE)
+    assert res["status"] == 0
+    _, _, flips = _check_layer(w, 0, res)
+    assert flips == 0
+
+
+@pytest.mark.parametrize("sf", [0, 1, 2])
+def test_decode_largest_routing(sf):
+    """1024 experts, 16 picks per token, 8 tokens: 128 token/expert pairs,
+    the largest decode plan; every score function."""
+    w = W.WORKLOADS["tiny"].with_(n_routed=1024, topk=16, m=8, score_func=sf)
+    dl = stage_layer(w, 0, experts_on_gpu=True)
     res = gpu_forward(dl, path=Q.MOE_PATH_DECODE)
     assert res["status"] == 0
     _, _, flips = _check_layer(w, 0, res)

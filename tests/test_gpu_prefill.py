@@ -179,6 +179,21 @@ def test_route_vl_softmax(m, path):
     assert np.any(ri_text != ri)
 
 
+@pytest.mark.parametrize("m", [1, 3])
+def test_wide_shapes_take_the_prefill_kernels_at_few_tokens(m):
+    """dim 7680 / inter 4096 (the largest widths the configuration allows):
+    the decode kernel's stages do not hold them, so MOE_PATH_AUTO runs every
+    call, even one token, on the prefill kernels."""
+    w = W.WORKLOADS["tiny"].with_(dim=7680, inter=4096, m=m)
+    cfg = lib_cfg(w)
+    assert Q.moe_v41_kernel_launches(cfg, 1, w.shared_kind) == Q.moe_v41_kernel_launches(
+        lib_cfg(w.with_(m=64)), 64, w.shared_kind) > 1
+    dl = stage_layer(w, 0, experts_on_gpu=True)
+    res = gpu_forward(dl)
+    assert res["status"] == 0
+    _check(w, 0, res)
+
+
 # ------------------------------------------------------ full-size prefill
 
 def _sample_tokens(w, res, n, must=()):
