@@ -279,6 +279,14 @@ __device__ __forceinline__ void load_xunit(XUnit& x, const int4* p) {
   x.s16[0] = v5.x; x.s16[1] = v5.y; x.s16[2] = v5.z; x.s16[3] = v5.w;
 }
 
+// (float)v for |v| < 2^22, exactly: v added to the bit pattern of 1.5 * 2^23
+// (whose binade has unit spacing), minus that value.  Two full-rate
+// instructions instead of one quarter-rate conversion.
+__device__ __forceinline__ float i2f_exact22(int v) { return __int_as_float(0x4B400000 + v) - 12582912.0f; }
+
+// byte j of v, zero-extended
+__device__ __forceinline__ int byte_of(uint32_t v, int j) { return (int)__byte_perm(v, 0u, 0x4440u + (uint32_t)j); }
+
 // Unit c of a Q2_K block (84 B, 4-B aligned, in shared memory) dotted with
 // the matching activation unit:
 //   sum_j dq_j * ( d * sc_j * sum(q * qx) - dmin * m_j * sum(qx) )
@@ -290,6 +298,10 @@ __device__ __forceinline__ float q2k_unit_dot(const uint8_t* blk, int c, const X
   const int h = c >> 1, half = c & 1;
   const uint32_t sa = w[2 * h], sb = w[2 * h + 1];
   const uint32_t dd = w[20];
+  // the scale / min bytes of sub-blocks j = 0..3 of this unit (bytes half,
+  // half + 2 of sa, then of sb), split into scale and min nibbles
+  const uint32_t sm = __byte_perm(sa, sb, half ? 0x7531u : 0x6420u);
+  const uint32_t sc4 = sm & 0x0F0F0F0Fu, mn4 = (sm >> 4) & 0x0F0F0F0Fu;
   float acc_d = 0.f, acc_m = 0.f;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -299,10 +311,9 @@ __device__ __forceinline__ float q2k_unit_dot(const uint8_t* blk, int c, const X
     a = dp4a_us(q2 & mask, x.q[4 * j + 2], a);
     a = dp4a_us(q3 & mask, x.q[4 * j + 3], a);
     const int isum = a >> (2 * j);
-    const uint32_t sw = (j < 2) ? sa : sb;
-    const uint32_t byte = (sw >> (8 * (half + 2 * (j & 1)))) & 0xFFu;
-    acc_d = fmaf(x.dq[j], (float)((int)(byte & 15u) * isum), acc_d);
-    acc_m = fmaf(x.dq[j], (float)((int)(byte >> 4) * x.s16[j]), acc_m);
+    // |sc * isum| <= 15 * 16 * 3 * 127 and |m * s16| <= 15 * 16 * 127: exact below 2^22
+    acc_d = fmaf(x.dq[j], i2f_exact22(byte_of(sc4, j) * isum), acc_d);
+    acc_m = fmaf(x.dq[j], i2f_exact22(byte_of(mn4, j) * x.s16[j]), acc_m);
   }
   const float d = half_bits_to_float(dd), dmin = half_bits_to_float(dd >> 16);
   return d * acc_d - dmin * acc_m;
@@ -338,6 +349,13 @@ __device__ __forceinline__ float q3k_unit_dot(const uint8_t* blk, int c, const X
   const uint32_t s_lo2 = __byte_perm(scw[1], scw[2], sel);  // scales bytes 4..7
   const uint32_t s_hi = __byte_perm(scw[2], scw[3], sel);   // scales bytes 8..11
   const uint32_t dbits = (a & 2u) ? (scw[3] >> 16) : (scw[3] & 0xFFFFu);
+  // six-bit scale codes of sub-blocks 8h + 2j + half, j = 0..3, one per byte:
+  // low four bits from bytes half, half + 2, half + 4, half + 6 of scales[0..7]
+  // (nibble h), high two bits from scales[8 + 2(j & 1) + half] at bit 4h + 2(j >> 1)
+  const uint32_t lo4 = (__byte_perm(s_lo, s_lo2, half ? 0x7531u : 0x6420u) >> (4 * h)) & 0x0F0F0F0Fu;
+  const uint32_t hv = __byte_perm(s_hi, s_hi, half ? 0x3131u : 0x2020u) >> (4 * h);
+  const uint32_t hi2 = ((hv & 0x0000FFFFu) | ((hv >> 2) & 0xFFFF0000u)) & 0x03030303u;
+  const uint32_t codes = lo4 | (hi2 << 4);
   float acc = 0.f;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -352,13 +370,8 @@ __device__ __forceinline__ float q3k_unit_dot(const uint8_t* blk, int c, const X
     b = dp4a_us(m[2] & hmask, x.q[4 * j + 2], b);
     b = dp4a_us(m[3] & hmask, x.q[4 * j + 3], b);
     const int isum = (a0 >> (2 * j)) + ((b >> (4 * h + j)) << 2) - 4 * x.s16[j];
-    // six-bit scale code of sub-block 8h + 2j + half
-    const int sbyte = 2 * j + half;  // 0..7
-    const uint32_t lo_src = sbyte < 4 ? s_lo : s_lo2;
-    const uint32_t lo4 = (lo_src >> (8 * (sbyte & 3) + 4 * h)) & 15u;
-    const uint32_t hi2 = (s_hi >> (8 * (2 * (j & 1) + half) + 2 * (2 * h + (j >> 1)))) & 3u;
-    const int scale = (int)(lo4 | (hi2 << 4)) - 32;
-    acc = fmaf(x.dq[j], (float)(scale * isum), acc);
+    // |scale * isum| <= 32 * 16 * 7 * 127: exact below 2^22
+    acc = fmaf(x.dq[j], i2f_exact22((byte_of(codes, j) - 32) * isum), acc);
   }
   return half_bits_to_float(dbits) * acc;
 }

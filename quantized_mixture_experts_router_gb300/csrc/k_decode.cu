@@ -96,6 +96,7 @@ struct Ctl {
   unsigned next;                  // consumer grab counter
   unsigned rdy;                   // RQ_* bits: inputs ready for every warp of the block
   unsigned xq;                    // consumer warps done with their share of q8_1(x)
+  unsigned sink;                  // status bits of the planner's warm-up pass (discarded)
 };
 
 __device__ __forceinline__ uint8_t* smem_base() {
@@ -373,7 +374,10 @@ __device__ __forceinline__ const DecodePlan* plan_of(const DecodeParams& p) {
 // computes the same plan; block 0 also writes the routing outputs).  Under
 // full load every dependent global round trip costs microseconds, so the
 // plan never goes through global memory.
-__device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t deadline) {
+// dry: the warm-up pass on whatever the workspace holds (the previous call's
+// keys): it writes only this block's shared-memory plan, which the real pass
+// overwrites before the plan barrier, and its status bits go to a sink.
+__device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t deadline, bool dry) {
   const uint32_t sel = p.sm_sel, plan_off = p.sm_plan;
   const int lane = threadIdx.x & 31;
   float* scratch = reinterpret_cast<float*>(smem_base() + sel);
@@ -381,8 +385,8 @@ __device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t 
   float* pk_w = reinterpret_cast<float*>(pk_id + MAXP);
   int* s_e = pk_id + 2 * MAXP;  // expert of each sorted position
   int* s_t = pk_id + 3 * MAXP;  // token of each sorted position
-  const bool writer = blockIdx.x == 0;
-  unsigned* status = &p.ctrl->status;
+  const bool writer = !dry && blockIdx.x == 0;
+  unsigned* status = dry ? &C.sink : &p.ctrl->status;
 #pragma unroll 1
   for (int t = 0; t < p.m; ++t) {
     float* wo = writer ? p.topk_w + (size_t)t * p.k : pk_w + t * p.k;
@@ -398,7 +402,8 @@ __device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t 
   }
   // the expert pointer table: the block's copy when there is one
   const unsigned long long* eptr = p.expert_ptrs;
-  if (p.ep_bytes) {
+  const uint32_t ep_bytes = dry ? 0u : p.ep_bytes;  // the copy may still be in flight during the warm-up
+  if (ep_bytes) {
     mbar_wait_bounded(bar(C.cbar[CB_EP]), 0u, deadline, &p.ctrl->status);
     __syncwarp();
   }
@@ -433,7 +438,7 @@ __device__ __noinline__ void build_plan(const DecodeParams& p, Ctl& C, uint64_t 
       bool bad = false;
       for (int j = 0; j < 3; ++j) {
         const size_t w = (size_t)e * 3 + j;
-        ptr[j] = (w + 1) * 8 <= p.ep_bytes ? eptr_s[w] : eptr[w];
+        ptr[j] = (w + 1) * 8 <= ep_bytes ? eptr_s[w] : eptr[w];
       }
       for (int j = 0; j < 3; ++j) bad |= (ptr[j] == 0ull) || (ptr[j] & 255ull);
       if (bad && writer) atomicOr(status, (unsigned)MOE_STATUS_MISSING_EXPERT);
@@ -735,6 +740,7 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     C.next = 0u;
     C.rdy = 0u;
     C.xq = 0u;
+    C.sink = 0u;
     fence_mbar_init();
   }
   __syncthreads();
@@ -746,11 +752,16 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     // Wait for every router row of the call, then build this block's plan.
     // On a timeout the plan is left empty (no routed expert work) so the
     // block still finishes; the status word already says why.
+    // The selection and plan code runs once per call, so its instructions are
+    // never cached when the routing is ready, and under the weight stream an
+    // instruction-cache miss costs about a microsecond: run it once on stale
+    // inputs while the router rows are computed.
+    build_plan(p, C, deadline, true);
     bool ok = true;
     if (lane == 0) ok = wait_count(&p.ctrl->router_done, (unsigned)z.n_router, deadline, &p.ctrl->status);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) {
-      build_plan(p, C, deadline);
+      build_plan(p, C, deadline, false);
     } else if (lane == 0) {
       DecodePlan* plan = reinterpret_cast<DecodePlan*>(smem_base() + p.sm_plan);
       plan->n_exp = 0;
