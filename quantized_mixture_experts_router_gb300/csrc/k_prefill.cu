@@ -485,6 +485,14 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
   }
   if (ncol <= 0) return;
   const int TN = (ncol + 15) & ~15;  // MMA width: a multiple of 16, <= TNM
+  // Split K-quant tiles whose four accumulators fit the 256 accumulator
+  // columns stack B_lo right after B_hi in the B stage: A_hi * [B_hi; B_lo]
+  // is then one MMA of width 2 TN (columns [0, TN) hi * hi, [TN, 2 TN)
+  // hi * lo), followed by A_lo * B_hi (width TN) onto columns [0, TN); the
+  // epilogue adds the two halves.  Two MMA instructions per matrix and K step
+  // instead of three.
+  const bool stack = SPLIT && PL::ATMEM && NMAT * 2 * TN <= 256;
+  const int mcols = stack ? 2 * TN : TN;  // accumulator columns of one matrix
   uint32_t ncols_tmem = 32;
   while (ncols_tmem < (uint32_t)(NMAT * TN)) ncols_tmem <<= 1;
   if (PL::ATMEM) ncols_tmem = 512;
@@ -685,7 +693,18 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
     for (int c0 = 16 * cg; c0 < TN; c0 += 16 * CG) {
       float v0[16], v1[16];
       tmem_ld16(tl + (uint32_t)c0, v0);
-      if (NMAT == 2) tmem_ld16(tl + (uint32_t)(TN + c0), v1);
+      if (NMAT == 2) tmem_ld16(tl + (uint32_t)(mcols + c0), v1);
+      if (stack) {
+        float w[16];
+        tmem_ld16(tl + (uint32_t)(TN + c0), w);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v0[j] += w[j];
+        if (NMAT == 2) {
+          tmem_ld16(tl + (uint32_t)(mcols + TN + c0), w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v1[j] += w[j];
+        }
+      }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int col = c0 + j;
@@ -755,7 +774,8 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
       }
 #pragma unroll
       for (int pt = 0; pt < PL::NPART; ++pt) {
-        const uint32_t dst = smem_u32(sm + PL::b_off(sb, pt));
+        const uint32_t dst = stack && pt == 1 ? smem_u32(sm + PL::b_off(sb, 0)) + (uint32_t)TN * 128u
+                                              : smem_u32(sm + PL::b_off(sb, pt));
         if constexpr (BMODE == B_GATHER) {
           for (int i = 0; i < TN; i += 4)
             tma_gather4(dst + (uint32_t)i * 128u, &g.map_b[pt], kc * KC, s_rows[i], s_rows[i + 1], s_rows[i + 2],
@@ -770,6 +790,7 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
   } else if (warp == W_MMA && lane == 0) {
     // ----------------------------------------------------- MMA issuer
     const uint32_t idesc = umma_idesc(TN, AK == A_BF16);
+    const uint32_t idesc2 = umma_idesc(2 * TN, AK == A_BF16);  // stacked: only when 2 TN <= 128
     for (int kc = 0; kc < nk; ++kc) {
       const int sb = kc % NSB, sa = KQ ? kc % NSA : sb;
       if (!mbar_wait_bounded(B(C.full_b[sb]), (uint32_t)((kc / NSB) & 1), deadline, g.status)) break;
@@ -778,13 +799,18 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
       const uint32_t base = smem_u32(sm);
 #pragma unroll
       for (int mat = 0; mat < NMAT; ++mat) {
-        const uint32_t td = tmem + (uint32_t)(mat * TN);
+        const uint32_t td = tmem + (uint32_t)(mat * mcols);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint64_t bh = umma_desc(base + PL::b_off(sb, 0) + 32u * k);
           if constexpr (PL::ATMEM) {
             // A in tensor memory: 8 columns (16 K values) per MMA
             const uint32_t ta = tmem + 256u + (uint32_t)(sa * PL::TA_COLS + (mat * PL::NPART) * 32 + 8 * k);
+            if (stack) {
+              umma_f16_ta(td, ta, bh, idesc2, (kc | k) ? 1u : 0u);  // A_hi * [B_hi; B_lo]
+              umma_f16_ta(td, ta + 32u, bh, idesc, 1u);            // A_lo * B_hi
+              continue;
+            }
             umma_f16_ta(td, ta, bh, idesc, (kc | k) ? 1u : 0u);
             if (SPLIT) {
               umma_f16_ta(td, ta, umma_desc(base + PL::b_off(sb, SPLIT ? 1 : 0) + 32u * k), idesc, 1u);
