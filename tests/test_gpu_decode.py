@@ -380,17 +380,18 @@ def test_argument_errors():
 
 # ------------------------------------------------------ full-size decode
 
-def test_decode_m1_full_shape_layers():
-    """The 40-layer decode workload's shape; three layers checked in full."""
+@pytest.mark.parametrize("layer", range(40))
+def test_decode_m1_full_shape_layers(layer):
+    """The 40-layer decode workload at full shape, every layer checked in full
+    (each layer's own seeded x, router, bias, experts and shared expert)."""
     w = W.WORKLOADS["decode_m1_40layer"]
-    for layer in (0, 17, 39):
-        dl = stage_layer(w, layer, experts_on_gpu=True)
-        res = gpu_forward(dl)
-        assert res["status"] == 0
-        _, _, flips = _check_layer(w, layer, res)
-        assert flips == 0
-        del dl
-        torch.cuda.empty_cache()
+    dl = stage_layer(w, layer, experts_on_gpu=True)
+    res = gpu_forward(dl)
+    assert res["status"] == 0
+    _, _, flips = _check_layer(w, layer, res)
+    assert flips == 0
+    del dl
+    torch.cuda.empty_cache()
 
 
 def test_decode_m8_kquant_shared_full_shape():
