@@ -256,6 +256,24 @@ def cpu_baseline(w: W.Workload, layers_per_step: int, n_units: int, threads: int
 
 # ------------------------------------------------------------------- GPU
 
+def max_over_ranks(vals, device=None):
+    """Each value's largest over the ranks of the process group (the job ends
+    when its slowest rank does); identity without a group of several ranks."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(world: int, m: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank moves m tokens per step through the
+    step's layers (weak scaling), over the slowest rank's time."""
+    return world * m * steps / (ms / 1000.0)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import quantized_mixture_experts_router_gb300 as Q
@@ -386,13 +404,9 @@ def run_ours(args, rank, world, local_rank):
         e2e = dict(ms=e_ms, steps=Ke, h2d=L * w.m * w.dim * 2, d2h=L * w.m * w.dim * 4)
 
     # max over ranks
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e["ms"] if e2e else 0.0], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
-        if e2e:
-            e2e["ms"] = float(t[1])
+    ms, e_ms_max = max_over_ranks([ms, e2e["ms"] if e2e else 0.0], dev)
+    if e2e:
+        e2e["ms"] = e_ms_max
     launches = Q.moe_v41_kernel_launches(cfg, w.m, w.shared_kind)
     del graph, layers, xs, out, tw, ti, ws
     torch.cuda.empty_cache()
@@ -471,7 +485,11 @@ def run_prefill(args, local_rank):
         torch.cuda.synchronize()
         e2e = dict(ms=e0.elapsed_time(e1), steps=K, h2d=w.m * w.dim * 2, d2h=w.m * w.dim * 4)
     launches = Q.moe_v41_kernel_launches(cfg, w.m, w.shared_kind)
-    return dict(w=w, K=K, per_call_ms=statistics.fmean(per_call), per_call_min_ms=min(per_call), distinct=distinct,
+    # the slowest rank's figures
+    mean_ms, min_ms, e_ms = max_over_ranks([statistics.fmean(per_call), min(per_call), e2e["ms"] if e2e else 0.0], dev)
+    if e2e:
+        e2e["ms"] = e_ms
+    return dict(w=w, K=K, per_call_ms=mean_ms, per_call_min_ms=min_ms, distinct=distinct,
                 clocks=clk, e2e=e2e, launches_per_call=launches)
 
 
@@ -644,9 +662,7 @@ def main():
             dist.destroy_process_group()
         return
     K = r["K"]
-    sec = r["ms"] / 1000.0
-    tokens = world * w.m * K  # each step moves m tokens through all L layers, per GPU
-    value = tokens / sec
+    value = job_tokens_per_s(world, w.m, K, r["ms"])
     traffic = recorded_traffic(args.workload)
     line = {
         "metric": metric_name(w), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -659,7 +675,7 @@ def main():
     }
     if r["e2e"]:
         e = r["e2e"]
-        line["e2e"] = {"value": world * w.m * e["steps"] / (e["ms"] / 1000.0), "unit": "tokens/s",
+        line["e2e"] = {"value": job_tokens_per_s(world, w.m, e["steps"], e["ms"]), "unit": "tokens/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
     if world == 1 and not args.no_cpu_baseline:
         tps, dt, n, desc = cpu_baseline(w, L, ncores, ncores, target_s=12.0)
@@ -667,8 +683,8 @@ def main():
                                 "sample": desc + f", {dt:.1f} s"}
     if pf:
         pw = pf["w"]
-        sec = pf["per_call_ms"] / 1000.0
-        p = {"workload": pw.name, "metric": metric_name(pw), "value": world * pw.m / sec, "unit": "tokens/s",
+        p = {"workload": pw.name, "metric": metric_name(pw), "value": job_tokens_per_s(world, pw.m, 1, pf["per_call_ms"]),
+             "unit": "tokens/s",
              "steps": pf["K"], "warmup": 3, "ms_per_step": pf["per_call_ms"], "ms_per_step_min": pf["per_call_min_ms"],
              "config": config_of(pw, 1, {"distinct": pf["distinct"], "resident": 1, "rotated": False,
                                          "resident_experts": args.resident_experts}),
@@ -679,7 +695,7 @@ def main():
              "dtype": "fp16 tensor-core GEMMs (gate/up split hi+lo), bf16 router/shared, f32 accumulate"}
         if pf["e2e"]:
             e = pf["e2e"]
-            p["e2e"] = {"value": world * pw.m * e["steps"] / (e["ms"] / 1000.0), "unit": "tokens/s",
+            p["e2e"] = {"value": job_tokens_per_s(world, pw.m, e["steps"], e["ms"]), "unit": "tokens/s",
                         "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
         if world == 1 and not args.no_cpu_baseline:
             tps, dt, n, desc = cpu_baseline(pw, 1, ncores, ncores, target_s=10.0)
