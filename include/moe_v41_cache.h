@@ -35,6 +35,10 @@
  * moe_v41_cache_reads after work that reads experts, so a slot is never
  * overwritten while enqueued work may still read it.
  *
+ * Errors: a call that returns MOE_ERR_ARG changed nothing.  After
+ * MOE_ERR_CUDA the host bookkeeping may no longer match the device tables:
+ * drain the streams and destroy the cache.
+ *
  * Simulation mode: with slots and tables both NULL the cache makes no CUDA
  * call at all; moe_v41_cache_fetch then only runs the replacement policy and
  * counts (hits, misses, evictions, bytes), e.g. to size the slot count from a
