@@ -563,7 +563,9 @@ def run_streamed(args, local_rank):
         stream = torch.cuda.current_stream()
         copy_stream = torch.cuda.Stream(device=dev)
         runs = []
-        for P in ([0, args.prefetch_k] if args.prefetch_k > 0 else [0]):
+        # each configuration twice, alternating: repetitions on one box have differed by up to 2.7x
+        plan_runs = [(rep, P) for rep in range(2) for P in ([0, args.prefetch_k] if args.prefetch_k > 0 else [0])]
+        for rep, P in plan_runs:
             slots = torch.empty((S, slot), dtype=torch.uint8, device=dev)
             tables = torch.empty((Ls, w.n_routed, 3), dtype=torch.int64, device=dev)
             cache = Q.ExpertCache(Ls, w.n_routed, S, slot, o1, o3, o2, arena, slots, tables)
@@ -595,7 +597,7 @@ def run_streamed(args, local_rank):
                 raise RuntimeError(f"device status {status} in the streamed leg")
             dd = {k: st1[k] - st0[k] for k in st1}
             calls = T * Ls
-            runs.append({"prefetch_k": P, "ms_per_layer_call": 1000.0 * sec / calls, "tokens_per_s": T / sec,
+            runs.append({"prefetch_k": P, "rep": rep, "ms_per_layer_call": 1000.0 * sec / calls, "tokens_per_s": T / sec,
                          "tokens_per_s_40_layers": T / sec * Ls / 40.0,
                          "hit_rate": dd["hits"] / max(1, dd["hits"] + dd["misses"]),
                          "prefetch_hits_per_call": dd["prefetch_hits"] / calls,
