@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
 
   if (tid == 0) {
     for (int s = 0; s < NSA; ++s) {
-      mbar_init(B(C.full_a[s]), NPROD);
+      mbar_init(B(C.full_a[s]), AK == A_Q2K ? NPROD / 2 : NPROD);  // Q2_K: half the producers fill a chunk
       mbar_init(B(C.empty_a[s]), 1);
     }
     for (int s = 0; s < NSB; ++s) {
@@ -543,6 +543,13 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
       auto ta_addr = [&](int sa, int m, int pt) -> uint32_t {
         return ta_lane + (uint32_t)(sa * PL::TA_COLS + (m * PL::NPART + pt) * 32);
       };
+      // Q2_K: producer half qd >> 1 fills chunk qd >> 1 of every unit, both
+      // plane halves jb of its sub-block position u (one tensor-memory wait
+      // and one hand-over per unit instead of two): its columns 16 jb + 8 u
+      const uint32_t ta_lane_u = tmem + 256u + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(8 * u);
+      auto ta_addr_q2 = [&](int sa, int m, int pt, int jb) -> uint32_t {
+        return ta_lane_u + (uint32_t)(16 * jb + sa * PL::TA_COLS + (m * PL::NPART + pt) * 32);
+      };
       // one K chunk: wait for the A stage, store this thread's piece, hand over
       auto chunk = [&](int kc, auto&& fillA) -> bool {
         const int sa = kc % NSA;
@@ -556,7 +563,14 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
 #pragma unroll
           for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-            for (int pt = 0; pt < PL::NPART; ++pt) tmem_st8(ta_addr(sa, m, pt), z);
+            for (int pt = 0; pt < PL::NPART; ++pt) {
+              if constexpr (AK == A_Q2K) {
+                tmem_st8(ta_addr_q2(sa, m, pt, 0), z);
+                tmem_st8(ta_addr_q2(sa, m, pt, 1), z);
+              } else {
+                tmem_st8(ta_addr(sa, m, pt), z);
+              }
+            }
         }
         tmem_wait_st();
         tc_fence_before();
@@ -583,31 +597,34 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
             sc[m][1] = rw[m][9];
             dd[m] = rw[m][10];
           }
-#pragma unroll
-          for (int cp = 0; cp < 2 && ok; ++cp) {
-            const int j = 2 * cp + jj;  // this thread's 2-bit plane
+          {
+            const int cp = jj;  // this thread's chunk of the unit (the producer half)
             ok = chunk(2 * v + cp, [&](int sa) {
 #pragma unroll
               for (int m = 0; m < NMAT; ++m) {
                 const float d = half_bits_to_float(dd[m]), dmin = half_bits_to_float(dd[m] >> 16);
-                const int sbi = 2 * j + u;  // sub-block 8h + sbi: scale byte sbi of the half
-                const uint32_t byte = (sc[m][sbi >> 2] >> (8 * (sbi & 3))) & 0xFFu;
-                uint32_t th0, th1, tl0 = 0, tl1 = 0;
-                q2k_tables<SPLIT>(d, dmin, byte, th0, th1, tl0, tl1);
-                uint32_t oh[8], ol[8];  // values l = 16u .. 16u + 15 in pairs: qs words 0..3 of the sub-block
 #pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                  const uint32_t qq = (qs[m][f] >> (2 * j)) & 0x03030303u;
-                  const uint32_t s0 = pair_sel(qq), s1 = pair_sel(qq >> 16);
-                  oh[2 * f] = prmt(th0, th1, s0);
-                  oh[2 * f + 1] = prmt(th0, th1, s1);
-                  if (SPLIT) {
-                    ol[2 * f] = prmt(tl0, tl1, s0);
-                    ol[2 * f + 1] = prmt(tl0, tl1, s1);
+                for (int jb = 0; jb < 2; ++jb) {
+                  const int j = 2 * cp + jb;  // 2-bit plane
+                  const int sbi = 2 * j + u;  // sub-block 8h + sbi: scale byte sbi of the half
+                  const uint32_t byte = (sc[m][sbi >> 2] >> (8 * (sbi & 3))) & 0xFFu;
+                  uint32_t th0, th1, tl0 = 0, tl1 = 0;
+                  q2k_tables<SPLIT>(d, dmin, byte, th0, th1, tl0, tl1);
+                  uint32_t oh[8], ol[8];  // values l = 16u .. 16u + 15 in pairs: qs words 0..3 of the sub-block
+#pragma unroll
+                  for (int f = 0; f < 4; ++f) {
+                    const uint32_t qq = (qs[m][f] >> (2 * j)) & 0x03030303u;
+                    const uint32_t s0 = pair_sel(qq), s1 = pair_sel(qq >> 16);
+                    oh[2 * f] = prmt(th0, th1, s0);
+                    oh[2 * f + 1] = prmt(th0, th1, s1);
+                    if (SPLIT) {
+                      ol[2 * f] = prmt(tl0, tl1, s0);
+                      ol[2 * f + 1] = prmt(tl0, tl1, s1);
+                    }
                   }
+                  tmem_st8(ta_addr_q2(sa, m, 0, jb), oh);
+                  if (SPLIT) tmem_st8(ta_addr_q2(sa, m, SPLIT ? 1 : 0, jb), ol);
                 }
-                tmem_st8(ta_addr(sa, m, 0), oh);
-                if (SPLIT) tmem_st8(ta_addr(sa, m, SPLIT ? 1 : 0), ol);
               }
             });
           }
