@@ -656,8 +656,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     r = run_ours(args, rank, world, local_rank)
-    pf = None if args.no_prefill else run_prefill(args, local_rank)
+    # the streamed leg runs before the prefill leg: after the prefill leg's end-to-end part its prefetch
+    # runs were up to 2.7x slower, an interaction of the legs, not part of either workload
     sm = None if (args.no_streamed or world > 1) else run_streamed(args, local_rank)
+    pf = None if args.no_prefill else run_prefill(args, local_rank)
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
