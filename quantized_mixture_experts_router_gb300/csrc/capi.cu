@@ -248,7 +248,7 @@ int moe_v41_forward_vl(const moe_v41_cfg* cfg, const void* x, int m, const void*
 int moe_v41_kernel_launches(const moe_v41_cfg* cfg, int m, int shared_kind) {
   if (check_cfg(cfg) != MOE_OK || m < 1 || m > cfg->max_tokens) return -1;
   if (shared_kind != MOE_SHARED_BF16 && shared_kind != MOE_SHARED_KQUANT) return -1;
-  if (use_decode(cfg, m)) return m <= DECODE_MAX_M ? 1 : -1;
+  if (use_decode(cfg, m)) return m <= DECODE_MAX_M && decode_fits(cfg->dim, cfg->inter) ? 1 : -1;
   return prefill_possible(*cfg) ? prefill_launches(shared_kind) : -1;
 }
 

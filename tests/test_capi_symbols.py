@@ -77,3 +77,10 @@ def test_kernel_launch_counts(lib):
     assert Q.moe_v41_kernel_launches(auto, 4097, Q.MOE_SHARED_BF16) == -1
     dec = Q.make_cfg(5120, 2304, 384, 6, max_tokens=16, path=Q.MOE_PATH_DECODE)
     assert Q.moe_v41_kernel_launches(dec, 9, Q.MOE_SHARED_BF16) == -1
+    # widths one decode stage does not hold: AUTO runs even a single token on the prefill kernels, and the
+    # workspace of such a configuration holds the prefill buffers although max_tokens <= 8
+    wide = Q.make_cfg(7680, 4096, 384, 6, max_tokens=1)
+    assert Q.moe_v41_kernel_launches(wide, 1, Q.MOE_SHARED_BF16) == 11
+    assert Q.moe_v41_workspace_bytes(wide) > Q.moe_v41_workspace_bytes(Q.make_cfg(5120, 2304, 384, 6, max_tokens=1))
+    wide_dec = Q.make_cfg(7680, 4096, 384, 6, max_tokens=1, path=Q.MOE_PATH_DECODE)
+    assert Q.moe_v41_kernel_launches(wide_dec, 1, Q.MOE_SHARED_BF16) == -1  # the forward refuses it too
