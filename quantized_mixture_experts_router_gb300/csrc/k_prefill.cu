@@ -374,6 +374,8 @@ struct Plan {
   }
 };
 
+constexpr int gcd_c(int a, int b) { return b == 0 ? a : gcd_c(b, a % b); }
+
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -411,9 +413,11 @@ __device__ __forceinline__ void q2k_tables(float d, float dmin, uint32_t scbyte,
   }
 }
 
-// PRMT selectors of two table entries: the 2-bit codes q0, q1 in bytes 0, 1
-// of qq select bytes (2q0, 2q0+1, 2q1, 2q1+1) of the 8-byte table.
-__device__ __forceinline__ uint32_t pair_sel(uint32_t qq) { return qq * 0x22u + 0x1010u; }
+// PRMT selectors of table entries: for the 2-bit codes q0..q3 in bytes 0..3
+// of qq, byte b of the result is (2qb + 1) << 4 | 2qb, so its low half selects
+// bytes (2q0, 2q0+1, 2q1, 2q1+1) of the 8-byte table and its high half the
+// same for q2, q3 (no byte carries into the next: 3 * 0x22 + 0x10 < 0x100).
+__device__ __forceinline__ uint32_t pair_sels(uint32_t qq) { return qq * 0x22u + 0x10101010u; }
 
 // q8_1 of one 32-value block of h held one value per lane: fp16 bits of
 // fp16(d) * q for this lane's value
@@ -614,7 +618,7 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
 #pragma unroll
                   for (int f = 0; f < 4; ++f) {
                     const uint32_t qq = (qs[m][f] >> (2 * j)) & 0x03030303u;
-                    const uint32_t s0 = pair_sel(qq), s1 = pair_sel(qq >> 16);
+                    const uint32_t s0 = pair_sels(qq), s1 = s0 >> 16;
                     oh[2 * f] = prmt(th0, th1, s0);
                     oh[2 * f + 1] = prmt(th0, th1, s1);
                     if (SPLIT) {
@@ -741,35 +745,80 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
   } else if (KQ && warp >= W_LOAD && warp < W_LOAD + NLW) {
     // ---------------------------------------------------- raw loaders
     if constexpr (KQ) {
+      // Word i of a buffer (row i / words, word i % words) goes to loader
+      // thread i % NLT, so each thread copies the same (row, word) pairs of
+      // every unit: their source offsets from the unit's first row are worked
+      // out once, and a copy costs an add, a compare and the cp.async.
+      constexpr int NLT = NLW * 32;
+      constexpr int WORDS = RG::words();
+      static_assert(TM * WORDS % NLT == 0, "loader threads tile the buffer");
       const int t = tid - W_LOAD * 32;
       const uint8_t* Am[2] = {A0, A1};
       const uint32_t raw_base = smem_u32(sm);
       const int nunits = nk / (AK == A_Q2K ? 2 : 4);
-      for (int v = 0; v < nunits; ++v) {
-        const int buf = v % RAWN;
-        // wait until every producer has read the unit that used this buffer
-        if (v >= RAWN && !mbar_wait_bounded(B(C.raw_free[buf]), (uint32_t)((v / RAWN - 1) & 1), deadline, g.status))
-          break;
+      const int lim = max(0, min(TM, g.a_rows - row0)) * WORDS;  // words of rows that exist
+      const size_t rb = g.a_row_bytes;
+      if constexpr (AK == A_Q2K) {
+        // buffer word w of a row: qs words 4 + 8h .. 4 + 8h + 7 of the
+        // super-block (w < 8), scale words 2h, 2h + 1 (w = 8, 9), d/dmin (w = 10)
+        constexpr int NJ = TM * WORDS / NLT;
+        uint32_t o0[NJ], o1[NJ];
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const uint32_t dst0 = raw_base + PL::raw_off(m, buf);
-          for (int idx = t; idx < TM * RG::words(); idx += NLW * 32) {
-            const int rr = idx / RG::words(), w = idx - rr * RG::words();
-            if (row0 + rr >= g.a_rows) continue;
-            const uint8_t* rowp = Am[m] + (size_t)(row0 + rr) * g.a_row_bytes;
-            const uint32_t* src;
-            if constexpr (AK == A_Q2K) {
-              const int b = v >> 1, h = v & 1;
-              const int bw = w < 8 ? 4 + 8 * h + w : (w < 10 ? 2 * h + (w - 8) : 20);
-              src = reinterpret_cast<const uint32_t*>(rowp + (size_t)b * Q2K_B) + bw;
-            } else {
-              const uintptr_t a = reinterpret_cast<uintptr_t>(rowp + (size_t)v * Q3K_B);
-              src = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3)) + w;
-            }
-            cp_async4(dst0 + (uint32_t)(rr * RG::PITCH + w) * 4u, src);
-          }
+        for (int j = 0; j < NJ; ++j) {
+          const int i = t + NLT * j, rr = i / WORDS, w = i - rr * WORDS;
+          const int b0 = w < 8 ? 4 + w : (w < 10 ? w - 8 : 20), dh = w < 8 ? 8 : (w < 10 ? 2 : 0);
+          o0[j] = (uint32_t)(rr * rb) + 4u * (uint32_t)b0;
+          o1[j] = o0[j] + 4u * (uint32_t)dh;
         }
-        cp_async_arrive(B(C.raw_full[buf]));  // once this thread's copies have landed
+        for (int v = 0; v < nunits; ++v) {
+          const int buf = v % RAWN;
+          if (v >= RAWN && !mbar_wait_bounded(B(C.raw_free[buf]), (uint32_t)((v / RAWN - 1) & 1), deadline, g.status))
+            break;
+          const bool hi = v & 1;
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m) {
+            const uint8_t* u = Am[m] + (size_t)row0 * rb + (size_t)(v >> 1) * Q2K_B;
+            const uint32_t dst = raw_base + PL::raw_off(m, buf) + 4u * (uint32_t)t;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j)
+              if (t + NLT * j < lim) cp_async4(dst + 4u * (uint32_t)(NLT * j), u + (hi ? o1[j] : o0[j]));
+          }
+          cp_async_arrive(B(C.raw_full[buf]));  // once this thread's copies have landed
+        }
+      } else {
+        // the words of a row start at its super-block's address rounded down
+        // to 4 bytes.  Copy j + P * q (P = WORDS / gcd(WORDS, NLT)) is copy j
+        // moved down by NLT * P / WORDS rows, so P offsets cover them all.
+        constexpr int P = WORDS / gcd_c(WORDS, NLT), NQ = TM * WORDS / (NLT * P), RQ = NLT * P / WORDS;
+        static_assert(TM * WORDS % (NLT * P) == 0, "whole periods per buffer");
+        uint32_t ro[P], wo[P], so[P];
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          const int i = t + NLT * j, rr = i / WORDS, w = i - rr * WORDS;
+          ro[j] = (uint32_t)(rr * rb);
+          wo[j] = 4u * (uint32_t)w;
+          so[j] = 4u * (uint32_t)(rr * RG::PITCH + w);
+        }
+        for (int v = 0; v < nunits; ++v) {
+          const int buf = v % RAWN;
+          if (v >= RAWN && !mbar_wait_bounded(B(C.raw_free[buf]), (uint32_t)((v / RAWN - 1) & 1), deadline, g.status))
+            break;
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m) {
+            const uintptr_t u0 = reinterpret_cast<uintptr_t>(Am[m] + (size_t)row0 * rb + (size_t)v * Q3K_B);
+            const uint32_t d0 = raw_base + PL::raw_off(m, buf);
+#pragma unroll 1
+            for (int q = 0; q < NQ; ++q) {
+              const uintptr_t u = u0 + (size_t)q * RQ * rb;
+              const uint32_t d = d0 + 4u * (uint32_t)(q * RQ * RG::PITCH);
+#pragma unroll
+              for (int j = 0; j < P; ++j)
+                if (t + NLT * (j + P * q) < lim)
+                  cp_async4(d + so[j], reinterpret_cast<const void*>(((u + ro[j]) & ~uintptr_t(3)) + wo[j]));
+            }
+          }
+          cp_async_arrive(B(C.raw_full[buf]));  // once this thread's copies have landed
+        }
       }
       // copies still in flight land before the block can exit
       asm volatile("cp.async.wait_all;" ::: "memory");
