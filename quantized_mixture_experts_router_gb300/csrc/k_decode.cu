@@ -724,7 +724,11 @@ __device__ __noinline__ void complete_item(const DecodeParams& p, Ctl& C, Item i
 __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__ DecodeParams p) {
   Ctl& C = *reinterpret_cast<Ctl*>(smem_base() + p.sm_ctl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
+  // Programmatic dependent launch: the next launch on the stream may start
+  // its blocks as this grid's blocks exit, and this grid touches no global
+  // memory before the previous launch has completed (the wait below).  Both
+  // are no-ops for a launch without the attribute.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(bar(C.full[i]), 1);
@@ -744,6 +748,8 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     fence_mbar_init();
   }
   __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
   const Sizes z = sizes_of(p);
   const int groups = p.D / DG;
 
@@ -1119,7 +1125,19 @@ int launch_decode_layer(const DecodeParams& p_in, int num_sms, cudaStream_t s) {
       return MOE_ERR_CUDA;
     attr_dev = dev;
   }
-  k_decode_layer<<<num_sms, NTH, p.smem_bytes, s>>>(p);
+  // programmatic stream serialisation: the block set-up of this call
+  // overlaps the tail of the previous launch on the stream
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)num_sms);
+  lc.blockDim = dim3(NTH);
+  lc.dynamicSmemBytes = p.smem_bytes;
+  lc.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, k_decode_layer, p) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
