@@ -248,8 +248,19 @@ __global__ void k_group_scatter(const int* __restrict__ idx, const float* __rest
 }
 
 // --------------------------------------------------------------- combine
+template <class V> __device__ __forceinline__ V vzero();
+template <> __device__ __forceinline__ float vzero<float>() { return 0.f; }
+template <> __device__ __forceinline__ float4 vzero<float4>() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+__device__ __forceinline__ float vfma(float w, float a, float c) { return fmaf(w, a, c); }
+__device__ __forceinline__ float4 vfma(float w, float4 a, float4 c) {
+  return make_float4(fmaf(w, a.x, c.x), fmaf(w, a.y, c.y), fmaf(w, a.z, c.z), fmaf(w, a.w, c.w));
+}
+__device__ __forceinline__ float vadd(float a, float b) { return a + b; }
+__device__ __forceinline__ float4 vadd(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+
 // out[t] = sum over t's usable pairs in ascending expert id of G * E, then
-// the shared expert's output
+// the shared expert's output (V = float4 where out is 16-byte aligned)
+template <class V, int VW = sizeof(V) / sizeof(float)>
 __global__ void k_combine(const int* __restrict__ idx, const int* __restrict__ pos_of,
                           const int* __restrict__ expert_ok, const float* __restrict__ pair_w,
                           const float* __restrict__ ep, const float* __restrict__ sp, const int* __restrict__ pos_sh,
@@ -281,11 +292,23 @@ __global__ void k_combine(const int* __restrict__ idx, const int* __restrict__ p
   }
   __syncthreads();
   const int n = s_n;
-  const float* sh = pos_sh ? ep + (size_t)pos_sh[t] * D : sp + (size_t)t * D;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.f;
-    for (int i = 0; i < n; ++i) acc = fmaf(s_w[i], ep[(size_t)s_pos[i] * D + d], acc);
-    out[(size_t)t * D + d] = acc + sh[d];
+  // VW values per access; every pair's value is loaded before the sums, so a
+  // thread has all its streams in flight at once
+  const int DV = D / VW;
+  const V* e = reinterpret_cast<const V*>(ep);
+  const V* sh = reinterpret_cast<const V*>(pos_sh ? ep + (size_t)pos_sh[t] * D : sp + (size_t)t * D);
+  V* o = reinterpret_cast<V*>(out + (size_t)t * D);
+  for (int c = threadIdx.x; c < DV; c += blockDim.x) {
+    V v[MAX_TOPK];
+#pragma unroll
+    for (int i = 0; i < MAX_TOPK; ++i)
+      if (i < n) v[i] = __ldcs(e + (size_t)s_pos[i] * DV + c);
+    const V hv = __ldcs(sh + c);
+    V acc = vzero<V>();
+#pragma unroll
+    for (int i = 0; i < MAX_TOPK; ++i)
+      if (i < n) acc = vfma(s_w[i], v[i], acc);
+    __stcs(o + c, vadd(acc, hv));
   }
 }
 
@@ -1062,7 +1085,12 @@ int launch_prefill(const PrefillParams& p, cudaStream_t s) {
       return rc;
   }
   // 8. ordered combine
-  k_combine<<<m, 256, 0, s>>>(p.topk_idx, pos_of, expert_ok, pair_w, ep, sp, shq ? pos_sh : nullptr, k, D, p.out);
+  if ((reinterpret_cast<uintptr_t>(p.out) & 15u) == 0)
+    k_combine<float4><<<m, 256, 0, s>>>(p.topk_idx, pos_of, expert_ok, pair_w, ep, sp, shq ? pos_sh : nullptr, k, D,
+                                        p.out);
+  else
+    k_combine<float><<<m, 256, 0, s>>>(p.topk_idx, pos_of, expert_ok, pair_w, ep, sp, shq ? pos_sh : nullptr, k, D,
+                                       p.out);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
