@@ -55,6 +55,39 @@ def test_tiny_prefill(m):
     _check(w, 0, res)
 
 
+@pytest.mark.parametrize("path,m", [("prefill", 37), ("decode", 3)])
+@pytest.mark.parametrize("shared", [W.SHARED_BF16, W.SHARED_KQUANT])
+def test_tiny_unaligned_out(path, m, shared):
+    """out needs only f32 alignment: one float past a 16-byte boundary the
+    prefill's ordered combine takes its scalar form, with the same sums bit
+    for bit (the decode kernel writes out by value)."""
+    pth = Q.MOE_PATH_PREFILL if path == "prefill" else Q.MOE_PATH_DECODE
+    w = W.WORKLOADS["tiny"].with_(m=m, shared_kind=shared)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    ref = gpu_forward(dl, path=pth)
+    cfg = lib_cfg(w, path=pth)
+    ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    Q.moe_v41_workspace_init(ws)
+    buf = torch.full((w.m * w.dim + 4,), float("nan"), dtype=torch.float32, device="cuda")
+    out = buf[1:1 + w.m * w.dim].view(w.m, w.dim)
+    assert out.data_ptr() % 16 == 4
+    tw = torch.empty((w.m, w.topk), dtype=torch.float32, device="cuda")
+    ti = torch.empty((w.m, w.topk), dtype=torch.int32, device="cuda")
+    Q.moe_v41_forward(cfg, dl.x, w.m, dl.router_w, dl.bias, dl.expert_ptrs, w.shared_kind, dl.sh1, dl.sh3, dl.sh2,
+                      out, tw, ti, None, ws)
+    assert Q.moe_v41_read_status(ws, clear=True) == 0
+    np.testing.assert_array_equal(out.cpu().numpy(), ref["out"])
+    np.testing.assert_array_equal(ti.cpu().numpy(), ref["topk_idx"])
+    # nothing written outside out
+    assert torch.isnan(buf[0]).item() and bool(torch.isnan(buf[1 + w.m * w.dim:]).all())
+    if path == "prefill":
+        _check(w, 0, ref)
+    else:
+        r = oracle_for(w, 0, given_logits=ref["logits"])
+        np.testing.assert_array_equal(ref["topk_idx"], r.topk_idx)
+        assert_close(ref["out"], r.out, "output")
+
+
 def test_tiny_prefill_auto_path_above_eight():
     w = W.WORKLOADS["tiny"].with_(m=33)
     dl = stage_layer(w, 1, experts_on_gpu=False)
