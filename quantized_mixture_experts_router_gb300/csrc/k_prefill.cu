@@ -54,30 +54,31 @@ __device__ __forceinline__ uint32_t f2h(float v) { return (uint32_t)__half_as_us
 // The q8_1 values of x, fp16(d) * q (exact in f32), as fp16 high and low
 // parts, written to the row of every (expert, token) pair of the token (and
 // of the K-quant shared expert's pair), so the gate/up GEMM reads its B
-// operand as contiguous rows.  One thread per block of 32 (the q8_1 rule:
-// d = amax / 127, q = round-half-away(v / d), d stored as fp16).
+// operand as contiguous rows.  Four threads per block of 32 (the q8_1 rule:
+// d = amax / 127, q = round-half-away(v / d), d stored as fp16), eight values
+// each, so that a warp's 16-byte stores cover 512 contiguous bytes.
 __global__ void k_xg(const uint16_t* __restrict__ x, int m, int D, int k, const int* __restrict__ pos_of,
                      const int* __restrict__ pos_sh, uint16_t* __restrict__ xgh, uint16_t* __restrict__ xgl) {
   const int nq = D / 32;
-  const long nb = (long)m * nq;
-  for (long g = blockIdx.x * (long)blockDim.x + threadIdx.x; g < nb; g += (long)gridDim.x * blockDim.x) {
-    const int t = (int)(g / nq), qb = (int)(g % nq);
-    const uint4* xp = reinterpret_cast<const uint4*>(x + g * 32);
-    uint32_t raw[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = __ldg(xp + i);
-      raw[4 * i + 0] = v.x; raw[4 * i + 1] = v.y; raw[4 * i + 2] = v.z; raw[4 * i + 3] = v.w;
-    }
+  const long nb = (long)m * nq * 4;  // quarter blocks; D / 8 per token, so a group of four never spans tokens
+  for (long g = blockIdx.x * (long)blockDim.x + threadIdx.x; g - (threadIdx.x & 31) < nb;
+       g += (long)gridDim.x * blockDim.x) {
+    const bool live = g < nb;
+    const long gq = live ? g : nb - 1;  // lanes past the end repeat the last quarter and store nothing
+    const int t = (int)(gq / (nq * 4));
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + gq);
+    const uint32_t raw[4] = {v.x, v.y, v.z, v.w};
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(raw[i])), fabsf(bf16hi(raw[i]))));
+    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(raw[i])), fabsf(bf16hi(raw[i]))));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const float d = __fdiv_rn(amax, 127.0f);
     const float rd = __frcp_rn(d);
     const float dq = __half2float(__float2half_rn(d));
-    uint32_t oh[16], ol[16];
+    uint32_t oh[4], ol[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 4; ++i) {
       const int q0 = amax == 0.0f ? 0 : q8_code(bf16lo(raw[i]), d, rd);
       const int q1 = amax == 0.0f ? 0 : q8_code(bf16hi(raw[i]), d, rd);
       const float v0 = dq * (float)q0, v1 = dq * (float)q1;
@@ -87,16 +88,13 @@ __global__ void k_xg(const uint16_t* __restrict__ x, int m, int D, int k, const 
       oh[i] = *reinterpret_cast<const uint32_t*>(&hh);
       ol[i] = *reinterpret_cast<const uint32_t*>(&ll);
     }
+    if (!live) continue;
+    const long off = gq - (long)t * nq * 4;  // 16-byte chunk of the token's row
     for (int i = 0; i <= k; ++i) {
       const int pos = i < k ? __ldg(pos_of + (size_t)t * k + i) : (pos_sh ? __ldg(pos_sh + t) : -1);
       if (pos < 0) continue;
-      uint4* ph = reinterpret_cast<uint4*>(xgh + (size_t)pos * D + qb * 32);
-      uint4* pl = reinterpret_cast<uint4*>(xgl + (size_t)pos * D + qb * 32);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        ph[c] = make_uint4(oh[4 * c], oh[4 * c + 1], oh[4 * c + 2], oh[4 * c + 3]);
-        pl[c] = make_uint4(ol[4 * c], ol[4 * c + 1], ol[4 * c + 2], ol[4 * c + 3]);
-      }
+      reinterpret_cast<uint4*>(xgh + (size_t)pos * D)[off] = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+      reinterpret_cast<uint4*>(xgl + (size_t)pos * D)[off] = make_uint4(ol[0], ol[1], ol[2], ol[3]);
     }
   }
 }
@@ -1035,7 +1033,7 @@ int launch_prefill(const PrefillParams& p, cudaStream_t s) {
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   // 4. the q8_1 values of x as fp16 high and low parts, in pair order
   {
-    const long nb = (long)m * (D / 32);
+    const long nb = (long)m * (D / 32) * 4;
     long blocks = (nb + 255) / 256;
     if (blocks > 152L * 8) blocks = 152L * 8;
     k_xg<<<(unsigned)blocks, 256, 0, s>>>(p.x, m, D, k, pos_of, shq ? pos_sh : nullptr, xgh, xgl);
