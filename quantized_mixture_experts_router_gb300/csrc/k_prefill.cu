@@ -1049,7 +1049,7 @@ int launch_prefill(const PrefillParams& p, cudaStream_t s) {
     g.tiles = gu_tiles; g.n_tiles = n_tiles; g.offsets = offsets; g.out_h = h16; g.out_ld = I;
     g.swiglu_limit = p.swiglu_limit; g.status = &p.ctrl->status; g.timeout_ns = p.timeout_ns;
     const unsigned grid = (unsigned)L.max_gu_tiles * (unsigned)(I / TM);
-    if ((rc = launch_gemm<A_Q2K, 2, true, E_SWIGLU_Q8, PF_TN_GU, 2, 4, 3, NP_KQ, B_TILED>(g, grid, s))) return rc;
+    if ((rc = launch_gemm<A_Q2K, 2, true, E_SWIGLU_Q8, PF_TN_GU, 2, 3, 3, NP_KQ, B_TILED>(g, grid, s))) return rc;
   }
   // 6. down -> E per pair
   {
