@@ -9,10 +9,13 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIBDIR = os.path.join(HERE, "_lib")
 
 
-def command():
+def command(src=None, out=None):
+    """The gcc command for the oracle library (src, out: another source and
+    library path, for the planted-mistake tests)."""
     os.makedirs(LIBDIR, exist_ok=True)
     return ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread",
-            os.path.join(HERE, "moe_oracle.c"), "-o", os.path.join(LIBDIR, "liboracle.so"), "-lm"]
+            src or os.path.join(HERE, "moe_oracle.c"), "-I", HERE, "-o", out or os.path.join(LIBDIR, "liboracle.so"),
+            "-lm"]
 
 
 def build() -> None:

@@ -177,6 +177,9 @@ def test_q8_1_zero_block_and_sum_field():
     x[0], x[1], x[2] = 127.0, 64.0, -3.0
     q = oracle.quantize_q8_1(x)
     assert oracle.f16_value(int(q[2]) | (int(q[3]) << 8)) == 188.0  # s = d * sum q, d = 1
+    q = oracle.quantize_q8_1(x * np.float32(0.125))
+    assert oracle.f16_value(int(q[0]) | (int(q[1]) << 8)) == 0.125
+    assert oracle.f16_value(int(q[2]) | (int(q[3]) << 8)) == 23.5  # the same codes, s = 188 / 8
 
 
 def test_q8_1_subnormal_scale():
@@ -487,6 +490,20 @@ def test_expert_matches_dense_library_matmul():
     hh = oracle.dequant_q8_1(oracle.quantize_q8_1(h), w.inter)
     E, _ = oracle.expert_kquant(cfg, xq8, w1, w3, w2)
     np.testing.assert_allclose(E, A2 @ hh, rtol=1e-12, atol=1e-12 * np.abs(A2 @ hh).max())
+
+
+def test_router_logits_match_a_library_matmul():
+    """z = x W_R^T on the bf16 values (the router step of the atlas page and
+    model.py Gate.forward), against numpy's f64 matmul rounded to f32; the
+    shapes differ in every dimension, so a transposed operand shows."""
+    rng = np.random.default_rng(5)
+    to_bf16 = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    x = to_bf16(rng.standard_normal((3, 256)))
+    R = to_bf16(rng.standard_normal((7, 256)) / 16)
+    f = lambda a: (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    z = oracle.router_logits(x, R)
+    assert z.shape == (3, 7) and z.dtype == np.float32
+    np.testing.assert_allclose(z, (f(x) @ f(R).T).astype(np.float32), rtol=2e-7, atol=0)
 
 
 def test_shared_bf16_matches_dense_library_matmul():
