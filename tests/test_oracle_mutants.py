@@ -60,6 +60,24 @@ MUTANTS = [
     ("routed_outputs_unweighted", "double g = (double)w[slot];", "double g = 1.0;"),
     ("shared_expert_dropped", "for (int d = 0; d < D; ++d) out[d] = y[d] + E[d];",
      "for (int d = 0; d < D; ++d) out[d] = y[d];"),
+    ("q2k_d_and_dmin_swapped", "double d = orc_f16_value((uint16_t)(blk[80] | (blk[81] << 8)));",
+     "double d = orc_f16_value((uint16_t)(blk[82] | (blk[83] << 8)));"),
+    ("q3k_hmask_bit_transposed", "int hb = (hmask[l] >> (4 * h + j)) & 1;", "int hb = (hmask[l] >> (h + 4 * j)) & 1;"),
+    ("q3k_upper_scales_low_nibble", "(scales12[b - 8] >> 4)", "(scales12[b - 8] & 15)"),
+    ("q8_1_signed_max", "float a = fabsf(xb[i]);", "float a = xb[i];"),
+    ("keys_ascending", "if (!na && ka != kb) return ka > kb;", "if (!na && ka != kb) return ka < kb;"),
+    ("no_epsilon", "sum += 1e-20f;", ""),
+    ("normalises_over_all_experts", "for (int i = 0; i < k; ++i) sum += w_out[i];",
+     "for (int i = 0; i < N; ++i) sum += s[i];"),
+    ("normalises_single_pick", "if (c->norm_topk_prob && k > 1) {", "if (c->norm_topk_prob) {"),
+    ("softmax_without_shift", "double mx = -INFINITY, sum = 0.0;\n    int any_nan = 0;\n    for (int e = 0; e < N; ++e) {\n"
+     "      float t = z[e] / c->gate_temp;\n      if (isnan(t)) any_nan = 1;\n      else if (t > mx) mx = t;\n",
+     "double mx = 0.0, sum = 0.0;\n    int any_nan = 0;\n    for (int e = 0; e < N; ++e) {\n"
+     "      float t = z[e] / c->gate_temp;\n      if (isnan(t)) any_nan = 1;\n"),
+    ("up_clamped_only_above", "if (u < -limit) { u = -limit; if (clipped) ++*clipped; }", ""),
+    ("clamps_at_zero_limit", "if (limit > 0) {", "if (limit >= 0) {"),
+    ("gate_and_up_swapped", "const uint8_t* w1 = L->experts[3 * e + 0];\n    const uint8_t* w3 = L->experts[3 * e + 1];",
+     "const uint8_t* w1 = L->experts[3 * e + 1];\n    const uint8_t* w3 = L->experts[3 * e + 0];"),
 ]
 
 

@@ -273,6 +273,20 @@ def test_routing_weights_sum_to_route_scale_and_ignore_bias():
     np.testing.assert_allclose(w[0] / w[0][0], s0 / s0[0], rtol=1e-6)
 
 
+@pytest.mark.parametrize("sf", [oracle.SCORE_SQRTSOFTPLUS, oracle.SCORE_SIGMOID])
+def test_routing_zero_scores_give_zero_weights(sf):
+    """Logits of -inf score 0 under sqrt-softplus and sigmoid: the keys are the
+    bias alone, and the weights are 0 / (0 + 1e-20) = 0, not 0 / 0 (the
+    renormalisation of metrale moe_v41.rs fn route_from_logits)."""
+    n, k = 12, 3
+    z = np.full((1, n), -np.inf, np.float32)
+    bias = np.linspace(-0.5, 0.6, n).astype(np.float32)[::-1].copy()
+    w, idx, nan = oracle.route_from_logits(_cfg_sf(n, k, sf), z, bias)
+    assert nan == 0
+    assert idx[0].tolist() == [0, 1, 2]
+    assert np.all(w == 0.0)
+
+
 def test_routing_nan_key_ranks_last():
     n = 8
     z = np.arange(n, dtype=np.float32)[None, :] * 3
@@ -312,6 +326,8 @@ def test_softmax_score_closed_forms():
     n = 16
     c = _cfg_sf(n, 2, oracle.SCORE_SOFTMAX)
     assert np.all(oracle.scores(c, np.full(n, 3.25, np.float32)) == np.float32(1.0 / n))
+    # equal logits far beyond exp's range are still 1/n each (softmax is shift invariant)
+    assert np.all(oracle.scores(c, np.full(n, 1000.0, np.float32)) == np.float32(1.0 / n))
     # one raised logit: e^a / (e^a + n - 1)
     z = np.zeros(n, np.float32)
     z[5] = 2.0
