@@ -148,7 +148,10 @@ MOE_API int moe_v41_route_vl(const moe_v41_cfg* cfg, const void* x, int m, const
  * persistent launch of integer-dot GEMVs); above that, at widths the decode
  * kernel does not take, or with MOE_PATH_PREFILL, the prefill kernels (tokens grouped by expert, tensor-core
  * GEMMs on dequantised tiles; router logits then carry the tensor cores' f32
- * accumulation order).
+ * accumulation order).  The decode launch allows programmatic stream
+ * serialisation: its blocks may set up while the previous launch on the
+ * stream finishes, and read or write no global memory before it has
+ * completed, so stream order holds as for any launch.
  *   x           bf16 [m, dim], 16-B aligned
  *   router_w    bf16 [n_routed, dim], 16-B aligned
  *   bias        f32 [n_routed]
