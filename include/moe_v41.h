@@ -194,13 +194,15 @@ MOE_API int moe_v41_forward_vl(const moe_v41_cfg* cfg, const void* x, int m, con
  *   workspace moe_v41_workspace_bytes(cfg) would need must fit in
  *   MOE_V41_NOALLOC_SCRATCH_BYTES, else MOE_ERR_WORKSPACE (the DeepSeek-V4.1
  *   shape, dim 5120 / inter 2304 / 384 experts / top-6 at 8 tokens, needs
- *   356 KB).  Nothing is allocated: no cudaMalloc, cudaFree or allocating
- *   library call.
- *   Set-up: the first call on a device (with that device current) looks up
- *   the array's device address once; make that first call before any stream
- *   capture.  Each call first clears the control words and counters it
- *   starts from.  All calls share the one array, so calls whose work overlaps
- *   on the GPU (different streams, or different host threads) race: serialise
+ *   381,952 bytes).  Nothing is allocated: no cudaMalloc, cudaFree or
+ *   allocating library call.
+ *   Set-up: every call looks the array's device address up on the current
+ *   device (cudaGetSymbolAddress, which allocates nothing).  The first call
+ *   on a device may load the library's device code there: make that first
+ *   call before any stream capture.  Each call first clears the control
+ *   words and counters it starts from.  All calls share the one array, so
+ *   calls whose work overlaps on the GPU (different streams, or different
+ *   host threads) race: serialise
  *   them, e.g. by issuing them on one stream. */
 MOE_API int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, int m, const void* router_w,
                                     const float* bias, const uint64_t* expert_ptrs, int shared_kind,

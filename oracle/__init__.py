@@ -80,6 +80,8 @@ def lib():
         L.orc_moe_layer.restype = i32
         L.orc_moe_layer.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Layer), vp, i32, vp, vp, vp, i32,
                                     ctypes.POINTER(Stats)]
+        L.orc_moe_layer_dense.restype = i32
+        L.orc_moe_layer_dense.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Layer), i32, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -274,3 +276,34 @@ def moe_layer(cfg: Cfg, x, router_w, bias, experts, shared_kind, sh1, sh3, sh2, 
     if rc != 0:
         raise RuntimeError(f"oracle layer failed with status {rc}")
     return LayerResult(out, w, idx, st.nan_keys, st.clipped)
+
+
+def moe_layer_dense(cfg: Cfg, x, router_w, bias, experts, shared_kind, sh1, sh3, sh2, given_logits=None,
+                    bias_vl=None, image_mask=None) -> LayerResult:
+    """The brute-force mode: every matrix dequantised to dense f64 up front,
+    textbook loops over all tokens.  Small inputs only (every expert must be
+    given).  clipped and nan_keys are not counted here (0)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    router_w = np.ascontiguousarray(router_w, dtype=np.uint16)
+    bias = np.ascontiguousarray(bias, dtype=np.float32)
+    m = x.shape[0]
+    keep = []
+    table = (ctypes.c_void_p * (3 * cfg.n_routed))()
+    for e in range(cfg.n_routed):
+        for j in range(3):
+            a = np.ascontiguousarray(experts[e][j], dtype=np.uint8)
+            keep.append(a)
+            table[3 * e + j] = a.ctypes.data
+    sh = [np.ascontiguousarray(s) for s in (sh1, sh3, sh2)]
+    gl = None if given_logits is None else np.ascontiguousarray(given_logits, dtype=np.float32)
+    bv = None if bias_vl is None else np.ascontiguousarray(bias_vl, dtype=np.float32)
+    im = None if image_mask is None else np.ascontiguousarray(image_mask, dtype=np.uint8)
+    L = Layer(_p(x), _p(router_w), _p(bias), _p(gl), ctypes.cast(table, ctypes.c_void_p), shared_kind,
+              _p(sh[0]), _p(sh[1]), _p(sh[2]), _p(bv), _p(im))
+    out = np.empty((m, cfg.dim), dtype=np.float64)
+    w = np.empty((m, cfg.topk), dtype=np.float32)
+    idx = np.empty((m, cfg.topk), dtype=np.int32)
+    rc = lib().orc_moe_layer_dense(ctypes.byref(cfg), ctypes.byref(L), m, _p(out), _p(w), _p(idx))
+    if rc != 0:
+        raise RuntimeError(f"dense oracle layer failed with status {rc}")
+    return LayerResult(out, w, idx, 0, 0)

@@ -483,3 +483,155 @@ int orc_moe_layer(const orc_cfg* c, const orc_layer* L, const int32_t* tokens, i
   if (stats) { stats->nan_keys = J.nan_keys; stats->clipped = J.clipped; }
   return J.status;
 }
+
+/* ------------------------------------------------------ brute-force mode */
+
+/* The whole layer a second way, for small inputs: every matrix of every
+ * expert (and the shared expert) is first dequantised to a dense f64 array,
+ * then the layer runs as textbook dense loops over all tokens at once.  The
+ * selection here takes k rounds of "the best remaining expert" (largest key,
+ * NaN last, lower id on equal keys) instead of a sort; the routed sum visits
+ * the experts in ascending id through a [m, N] weight matrix that is zero
+ * where a token did not pick.  Same formulas as orc_moe_layer ([MoE atlas]
+ * Router / Routed expert / Shared expert steps; [moe_v41.rs]
+ * route_from_logits), composed independently; the two must agree to
+ * rounding of the f64 sums.  Memory: 8 * (3 * N * D * I + 3 * D * I) bytes. */
+int orc_moe_layer_dense(const orc_cfg* c, const orc_layer* L, int m, double* out, float* topk_w,
+                        int32_t* topk_idx) {
+  const int D = c->dim, I = c->inter, N = c->n_routed, k = c->topk;
+  if (D % 256 || I % 256 || k < 1 || k > N) return ORC_ERR_ARG;
+  for (int e = 0; e < N; ++e)
+    for (int j = 0; j < 3; ++j)
+      if (!L->experts[3 * e + j]) return ORC_ERR_MISSING_EXPERT;
+  const size_t DI = (size_t)D * I;
+  double* W1 = (double*)malloc(sizeof(double) * DI * N);
+  double* W3 = (double*)malloc(sizeof(double) * DI * N);
+  double* W2 = (double*)malloc(sizeof(double) * DI * N);
+  double* S1 = (double*)malloc(sizeof(double) * DI);
+  double* S3 = (double*)malloc(sizeof(double) * DI);
+  double* S2 = (double*)malloc(sizeof(double) * DI);
+  double* X = (double*)malloc(sizeof(double) * (size_t)m * D);   /* bf16 x, exact */
+  double* XQ = (double*)malloc(sizeof(double) * (size_t)m * D);  /* q8_1(x) values */
+  float* Z = (float*)malloc(sizeof(float) * (size_t)m * N);
+  double* G = (double*)calloc((size_t)m * N, sizeof(double));   /* routing weight, 0 = not picked */
+  /* 1. every matrix, dense */
+  for (int e = 0; e < N; ++e) {
+    orc_dequant_matrix(2, L->experts[3 * e + 0], I, D, W1 + DI * e);
+    orc_dequant_matrix(2, L->experts[3 * e + 1], I, D, W3 + DI * e);
+    orc_dequant_matrix(3, L->experts[3 * e + 2], D, I, W2 + DI * e);
+  }
+  if (L->shared_kind == ORC_SHARED_BF16) {
+    for (size_t i = 0; i < DI; ++i) {
+      S1[i] = orc_bf16_value(((const uint16_t*)L->sh1)[i]);
+      S3[i] = orc_bf16_value(((const uint16_t*)L->sh3)[i]);
+      S2[i] = orc_bf16_value(((const uint16_t*)L->sh2)[i]);
+    }
+  } else {
+    orc_dequant_matrix(2, (const uint8_t*)L->sh1, I, D, S1);
+    orc_dequant_matrix(2, (const uint8_t*)L->sh3, I, D, S3);
+    orc_dequant_matrix(3, (const uint8_t*)L->sh2, D, I, S2);
+  }
+  /* 2. activations: bf16 values and their q8_1 values */
+  {
+    float* xf = (float*)malloc(sizeof(float) * D);
+    uint8_t* q8 = (uint8_t*)malloc((size_t)36 * (D / 32));
+    for (int t = 0; t < m; ++t) {
+      for (int d = 0; d < D; ++d) {
+        X[(size_t)t * D + d] = orc_bf16_value(L->x[(size_t)t * D + d]);
+        xf[d] = (float)X[(size_t)t * D + d];
+      }
+      orc_quantize_q8_1(xf, D, q8);
+      orc_dequant_q8_1(q8, D, XQ + (size_t)t * D);
+    }
+    free(xf); free(q8);
+  }
+  /* 3. logits: Z = X W_R^T (f64 sums handed on as f32), unless given */
+  for (int t = 0; t < m; ++t)
+    for (int e = 0; e < N; ++e) {
+      if (L->given_logits) { Z[(size_t)t * N + e] = L->given_logits[(size_t)t * N + e]; continue; }
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d) acc += X[(size_t)t * D + d] * orc_bf16_value(L->router_w[(size_t)e * D + d]);
+      Z[(size_t)t * N + e] = (float)acc;
+    }
+  /* 4. selection by k rounds of the best remaining key, then the weights */
+  {
+    float* s = (float*)malloc(sizeof(float) * N);
+    float* key = (float*)malloc(sizeof(float) * N);
+    char* taken = (char*)malloc((size_t)N);
+    for (int t = 0; t < m; ++t) {
+      const float* b = (L->image_mask && L->bias_vl && L->image_mask[t]) ? L->bias_vl : L->bias;
+      orc_scores(c, Z + (size_t)t * N, s);
+      for (int e = 0; e < N; ++e) { key[e] = s[e] + b[e]; taken[e] = 0; }
+      float* w = topk_w + (size_t)t * k;
+      int32_t* ix = topk_idx + (size_t)t * k;
+      for (int i = 0; i < k; ++i) {
+        int best = -1;
+        for (int e = 0; e < N; ++e) {
+          if (taken[e]) continue;
+          if (best < 0) { best = e; continue; }
+          int en = isnan(key[e]), bn = isnan(key[best]);
+          if (en) continue;                               /* NaN never beats anything */
+          if (bn || key[e] > key[best]) best = e;         /* ids ascend: equal keys keep the lower */
+        }
+        taken[best] = 1;
+        ix[i] = best;
+        w[i] = s[best];
+      }
+      /* renormalised over the picks (in pick order, f32) when asked and k > 1 */
+      const int renorm = c->norm_topk_prob != 0 && k >= 2;
+      float denom = 0.0f;
+      for (int i = 0; i < k && renorm; ++i) denom += w[i];
+      denom = denom + 1e-20f;
+      for (int i = 0; i < k; ++i) {
+        if (renorm) w[i] = w[i] / denom;
+        w[i] *= c->route_scale;
+        G[(size_t)t * N + ix[i]] = (double)w[i];
+      }
+    }
+    free(s); free(key); free(taken);
+  }
+  /* 5. dense expert FFNs; y[t] = sum over e ascending of G[t, e] E_e[t],
+   *    then the shared expert */
+  {
+    double* hv = (double*)malloc(sizeof(double) * I);
+    float* hf = (float*)malloc(sizeof(float) * I);
+    uint8_t* hq = (uint8_t*)malloc((size_t)36 * (I / 32));
+    for (int t = 0; t < m; ++t) {
+      double* o = out + (size_t)t * D;
+      const double* xq = XQ + (size_t)t * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      for (int e = 0; e <= N; ++e) {          /* e == N: the shared expert */
+        const int shared = e == N;
+        if (!shared && G[(size_t)t * N + e] == 0.0) continue;
+        const double* A1 = shared ? S1 : W1 + DI * e;
+        const double* A3 = shared ? S3 : W3 + DI * e;
+        const double* A2 = shared ? S2 : W2 + DI * e;
+        const int bf = shared && L->shared_kind == ORC_SHARED_BF16;
+        const double* xin = bf ? X + (size_t)t * D : xq;
+        for (int r = 0; r < I; ++r) {
+          double g = 0.0, u = 0.0;
+          for (int d = 0; d < D; ++d) {
+            g += A1[(size_t)r * D + d] * xin[d];
+            u += A3[(size_t)r * D + d] * xin[d];
+          }
+          hf[r] = (float)orc_swiglu(g, u, c->swiglu_limit, NULL);
+        }
+        if (bf) {
+          for (int r = 0; r < I; ++r) hv[r] = orc_bf16_value(orc_bf16_from_f32(hf[r]));
+        } else {
+          orc_quantize_q8_1(hf, I, hq);
+          orc_dequant_q8_1(hq, I, hv);
+        }
+        const double gw = shared ? 1.0 : G[(size_t)t * N + e];
+        for (int d = 0; d < D; ++d) {
+          double acc = 0.0;
+          for (int j = 0; j < I; ++j) acc += A2[(size_t)d * I + j] * hv[j];
+          o[d] += gw * acc;
+        }
+      }
+    }
+    free(hv); free(hf); free(hq);
+  }
+  free(W1); free(W3); free(W2); free(S1); free(S3); free(S2); free(X); free(XQ); free(Z); free(G);
+  return ORC_OK;
+}

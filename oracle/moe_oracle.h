@@ -65,5 +65,9 @@ void orc_shared_bf16(const orc_cfg* c, const uint16_t* x, const uint16_t* w1, co
                      const uint16_t* w2, double* S, int* clipped);
 int orc_moe_layer(const orc_cfg* c, const orc_layer* L, const int32_t* tokens, int n_tok, double* out,
                   float* topk_w, int32_t* topk_idx, int nthreads, orc_stats* stats);
+/* Brute-force mode for small inputs: dense f64 matrices up front, textbook
+ * loops over all m tokens (no token subset, no threads). */
+int orc_moe_layer_dense(const orc_cfg* c, const orc_layer* L, int m, double* out, float* topk_w,
+                        int32_t* topk_idx);
 
 #endif

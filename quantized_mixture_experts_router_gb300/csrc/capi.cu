@@ -9,19 +9,6 @@ namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-int check_cfg(const moe_v41_cfg* c) {
-  if (!c) return MOE_ERR_ARG;
-  if (c->dim < 256 || c->dim > 7680 || c->dim % 256) return MOE_ERR_ARG;
-  if (c->inter < 256 || c->inter > 7680 || c->inter % 256) return MOE_ERR_ARG;
-  if (c->n_routed < 1 || c->n_routed > MAX_N) return MOE_ERR_ARG;
-  if (c->topk < 1 || c->topk > MAX_TOPK || c->topk > c->n_routed) return MOE_ERR_ARG;
-  if (!(c->gate_temp > 0.0f)) return MOE_ERR_ARG;
-  if (c->max_tokens < 1 || c->max_tokens > 65536) return MOE_ERR_ARG;
-  if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_PREFILL) return MOE_ERR_ARG;
-  if (c->score_func < MOE_SCORE_SQRTSOFTPLUS || c->score_func > MOE_SCORE_SOFTMAX) return MOE_ERR_ARG;
-  return MOE_OK;
-}
-
 int check_ws(const moe_v41_cfg* c, void* ws, size_t ws_bytes) {
   if (!ws) return MOE_ERR_WORKSPACE;
   if (!aligned(ws, 256)) return MOE_ERR_ALIGN;

@@ -87,6 +87,21 @@ struct PrefillParams {
   unsigned long long timeout_ns;
 };
 
+// Configuration checks every entry point starts with: MOE_OK, or MOE_ERR_ARG
+// for a value out of the ranges include/moe_v41.h states.
+inline int check_cfg(const moe_v41_cfg* c) {
+  if (!c) return MOE_ERR_ARG;
+  if (c->dim < 256 || c->dim > 7680 || c->dim % 256) return MOE_ERR_ARG;
+  if (c->inter < 256 || c->inter > 7680 || c->inter % 256) return MOE_ERR_ARG;
+  if (c->n_routed < 1 || c->n_routed > MAX_N) return MOE_ERR_ARG;
+  if (c->topk < 1 || c->topk > MAX_TOPK || c->topk > c->n_routed) return MOE_ERR_ARG;
+  if (!(c->gate_temp > 0.0f)) return MOE_ERR_ARG;
+  if (c->max_tokens < 1 || c->max_tokens > 65536) return MOE_ERR_ARG;
+  if (c->path < MOE_PATH_AUTO || c->path > MOE_PATH_PREFILL) return MOE_ERR_ARG;
+  if (c->score_func < MOE_SCORE_SQRTSOFTPLUS || c->score_func > MOE_SCORE_SOFTMAX) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
 int launch_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols, void* q8, cudaStream_t s);
 int launch_select(const SelectParams& p, cudaStream_t s);
 int launch_route_decode(const RouteParams& p, cudaStream_t s);

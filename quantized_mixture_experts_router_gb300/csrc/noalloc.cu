@@ -2,8 +2,6 @@
 // a fixed array that the library itself holds on each GPU, for callers that
 // cannot allocate device memory (see include/moe_v41.h).  It launches the same
 // fused decode kernel as moe_v41_forward; only where the scratch lives differs.
-#include <mutex>
-
 #include "internal.h"
 
 using namespace moe;
@@ -11,25 +9,17 @@ using namespace moe;
 namespace {
 
 // The scratch.  Every GPU that loads the library holds these bytes until the
-// process exits.  Kernels receive its device address, obtained once per
-// device with cudaGetSymbolAddress; host code never dereferences the symbol.
+// process exits.  Kernels receive its device address, which host code looks
+// up on every call with cudaGetSymbolAddress (no allocation; it stays correct
+// if the device's context is torn down and the module reloaded at another
+// address); host code never dereferences the symbol itself.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_V41_NOALLOC_SCRATCH_BYTES];
 
-constexpr int MAX_DEVICES = 64;
-std::mutex g_setup_mu;
-void* g_scratch_addr[MAX_DEVICES] = {};
-
-// Device address of the scratch on the current device (set up on first use).
+// Device address of the scratch on the current device.
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return MOE_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+  *out = p;
   return MOE_OK;
 }
 
@@ -42,14 +32,11 @@ extern "C" int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, in
                                        const void* sh_w1, const void* sh_w3, const void* sh_w2, float* out,
                                        float* topk_w, int32_t* topk_idx, float* logits_out, uint32_t* status_out,
                                        void* stream) {
-  if (!cfg) return MOE_ERR_ARG;
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
   const moe_v41_cfg& c = *cfg;
-  if (c.dim < 256 || c.dim % 256 || c.inter < 256 || c.inter % 256) return MOE_ERR_ARG;
-  if (c.n_routed < 1 || c.n_routed > MAX_N || c.topk < 1 || c.topk > MAX_TOPK || c.topk > c.n_routed)
-    return MOE_ERR_ARG;
-  if (!(c.gate_temp > 0.0f) || c.max_tokens < 1 || c.max_tokens > DECODE_MAX_M) return MOE_ERR_ARG;
-  if (c.path == MOE_PATH_PREFILL) return MOE_ERR_ARG;
-  if (c.score_func < MOE_SCORE_SQRTSOFTPLUS || c.score_func > MOE_SCORE_SOFTMAX) return MOE_ERR_ARG;
+  // the decode kernels only: at most eight tokens, never the prefill path
+  if (c.max_tokens > DECODE_MAX_M || c.path == MOE_PATH_PREFILL) return MOE_ERR_ARG;
   if (m < 1 || m > c.max_tokens) return MOE_ERR_ARG;
   if (!x || !router_w || !bias || !expert_ptrs || !sh_w1 || !sh_w3 || !sh_w2 || !out || !topk_w || !topk_idx)
     return MOE_ERR_ARG;
@@ -61,7 +48,7 @@ extern "C" int moe_v41_forward_noalloc(const moe_v41_cfg* cfg, const void* x, in
   if (L.total > (size_t)MOE_V41_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;  // beyond the fixed scratch
 
   void* base = nullptr;
-  int rc = scratch_address(&base);
+  rc = scratch_address(&base);
   if (rc) return rc;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||

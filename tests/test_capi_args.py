@@ -80,3 +80,42 @@ def test_out_needs_no_more_than_f32_alignment(Q):
 def test_error_strings(Q):
     for code in (Q.MOE_ERR_ARG, Q.MOE_ERR_ALIGN, Q.MOE_ERR_WORKSPACE, Q.MOE_ERR_CUDA):
         assert Q.strerror(code) and Q.strerror(code) != Q.strerror(Q.MOE_OK)
+
+
+def _noalloc(Q, cfg, **kw):
+    a = dict(x=A, m=1, router_w=A, bias=A, ep=A, shared=0, sh1=A, sh3=A, sh2=A, out=A, tw=A, ti=A, lg=None, st=None)
+    a.update(kw)
+    return Q.lib().moe_v41_forward_noalloc(ctypes.byref(cfg), a["x"], a["m"], a["router_w"], a["bias"], a["ep"],
+                                           a["shared"], a["sh1"], a["sh3"], a["sh2"], a["out"], a["tw"], a["ti"],
+                                           a["lg"], a["st"], None)
+
+
+def test_noalloc_rejects_what_the_plain_forward_rejects(Q):
+    """The allocation-free forward checks the configuration exactly like
+    moe_v41_forward, plus its own limits (decode kernels only: at most eight
+    tokens, never the prefill path), before any CUDA call."""
+    for bad in (dict(dim=300), dict(topk=0), dict(n_routed=1025), dict(gate_temp=0.0), dict(max_tokens=0),
+                dict(path=3), dict(path=-1), dict(score_func=3)):
+        assert _noalloc(Q, _cfg(Q, **bad)) == Q.MOE_ERR_ARG, bad
+        assert _forward(Q, _cfg(Q, **bad)) == Q.MOE_ERR_ARG, bad
+    assert _noalloc(Q, _cfg(Q, max_tokens=9)) == Q.MOE_ERR_ARG
+    assert _noalloc(Q, _cfg(Q, path=Q.MOE_PATH_PREFILL)) == Q.MOE_ERR_ARG
+    cfg = _cfg(Q, max_tokens=4)
+    assert _noalloc(Q, cfg, m=0) == Q.MOE_ERR_ARG
+    assert _noalloc(Q, cfg, m=5) == Q.MOE_ERR_ARG
+    for name in ("x", "router_w", "bias", "ep", "sh1", "sh3", "sh2", "out", "tw", "ti"):
+        assert _noalloc(Q, cfg, **{name: None}) == Q.MOE_ERR_ARG, name
+    assert _noalloc(Q, cfg, shared=2) == Q.MOE_ERR_ARG
+    for name, off in (("x", 8), ("router_w", 8), ("ep", 4), ("sh1", 128)):
+        assert _noalloc(Q, cfg, **{name: A + off}) == Q.MOE_ERR_ALIGN, name
+
+
+def test_noalloc_scratch_figure_of_the_header(Q):
+    """include/moe_v41.h states the scratch the DeepSeek-V4.1 shape needs at
+    eight tokens; it must fit the fixed array, and a shape that needs more is
+    refused before any CUDA call."""
+    ds = _cfg(Q, dim=5120, inter=2304, n_routed=384, topk=6, max_tokens=8)
+    assert Q.moe_v41_workspace_bytes(ds) == 381952 <= Q.NOALLOC_SCRATCH_BYTES
+    big = _cfg(Q, dim=5120, inter=2560, n_routed=1024, topk=16, max_tokens=8)
+    assert Q.moe_v41_workspace_bytes(big) > Q.NOALLOC_SCRATCH_BYTES
+    assert _noalloc(Q, big) == Q.MOE_ERR_WORKSPACE

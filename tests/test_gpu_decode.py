@@ -325,10 +325,12 @@ def test_wait_timeout_sets_status_and_returns():
     assert_close(good["out"], r.out, "output after a timed-out call")
 
 
-def test_graph_replay_matches_eager():
+def test_graph_replay_matches_eager_and_the_oracle():
     """A decode step (three layer calls) captured as a CUDA graph and replayed
-    gives the eager launches' results bit for bit: the call has no host round
-    trip, and the kernel resets its call-wide counters itself."""
+    gives the eager launches' results bit for bit (the call has no host round
+    trip, and the kernel resets its call-wide counters itself), and every
+    replayed layer's output is within the parity bars of the oracle run on
+    the replay's own logits."""
     w = W.WORKLOADS["tiny"].with_(m=3)
     layers = [stage_layer(w, l, experts_on_gpu=False) for l in range(3)]
     cfg = lib_cfg(w, path=Q.MOE_PATH_DECODE)
@@ -337,17 +339,21 @@ def test_graph_replay_matches_eager():
     outs = [torch.empty((w.m, w.dim), device="cuda") for _ in layers]
     tws = [torch.empty((w.m, w.topk), device="cuda") for _ in layers]
     tis = [torch.empty((w.m, w.topk), dtype=torch.int32, device="cuda") for _ in layers]
+    lgs = [torch.empty((w.m, w.n_routed), device="cuda") for _ in layers]
 
     def step():
         for l, d in enumerate(layers):
             Q.moe_v41_forward(cfg, d.x, w.m, d.router_w, d.bias, d.expert_ptrs, w.shared_kind, d.sh1, d.sh3, d.sh2,
-                              outs[l], tws[l], tis[l], None, ws)
+                              outs[l], tws[l], tis[l], lgs[l], ws)
 
     step()
     torch.cuda.synchronize()
     eager = [(o.clone(), t.clone(), i.clone()) for o, t, i in zip(outs, tws, tis)]
-    for o in outs:
+    for o, t, i, g in zip(outs, tws, tis, lgs):
         o.zero_()
+        t.zero_()
+        i.zero_()
+        g.zero_()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         step()
@@ -357,6 +363,59 @@ def test_graph_replay_matches_eager():
     assert Q.moe_v41_read_status(ws, clear=True) == 0
     for (eo, et, ei), o, t, i in zip(eager, outs, tws, tis):
         assert torch.equal(eo, o) and torch.equal(et, t) and torch.equal(ei, i)
+    for l in range(len(layers)):
+        res = dict(out=outs[l].cpu().numpy(), topk_w=tws[l].cpu().numpy(), topk_idx=tis[l].cpu().numpy(),
+                   logits=lgs[l].cpu().numpy())
+        _, _, flips = _check_layer(w, l, res)
+        assert flips == 0
+
+
+def test_graph_replay_full_shape_step_matches_the_oracle():
+    """The 40-layer decode step as the bench runs it (one CUDA graph of the
+    layer calls, all 40 layers' experts resident), replayed twice: every
+    layer's replayed output, weights and picks are checked against the
+    oracle on the replay's own logits."""
+    w = W.WORKLOADS["decode_m1_40layer"]
+    n_layers = 40
+    free, _ = torch.cuda.mem_get_info()
+    from synth.device import slot_layout
+    need = n_layers * w.n_routed * slot_layout(w)[3] + (4 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB of free device memory")
+    layers = [stage_layer(w, l, experts_on_gpu=True) for l in range(n_layers)]
+    cfg = lib_cfg(w)
+    ws = torch.empty(Q.moe_v41_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    Q.moe_v41_workspace_init(ws)
+    outs = [torch.empty((w.m, w.dim), device="cuda") for _ in layers]
+    tws = [torch.empty((w.m, w.topk), device="cuda") for _ in layers]
+    tis = [torch.empty((w.m, w.topk), dtype=torch.int32, device="cuda") for _ in layers]
+    lgs = [torch.empty((w.m, w.n_routed), device="cuda") for _ in layers]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        Q.moe_v41_forward(cfg, layers[0].x, w.m, layers[0].router_w, layers[0].bias, layers[0].expert_ptrs,
+                          w.shared_kind, layers[0].sh1, layers[0].sh3, layers[0].sh2, outs[0], tws[0], tis[0],
+                          lgs[0], ws, stream=s)
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for l, d in enumerate(layers):
+                Q.moe_v41_forward(cfg, d.x, w.m, d.router_w, d.bias, d.expert_ptrs, w.shared_kind, d.sh1, d.sh3,
+                                  d.sh2, outs[l], tws[l], tis[l], lgs[l], ws, stream=s)
+    for o in outs:
+        o.zero_()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert Q.moe_v41_read_status(ws, clear=True) == 0
+    for l in range(n_layers):
+        res = dict(out=outs[l].cpu().numpy(), topk_w=tws[l].cpu().numpy(), topk_idx=tis[l].cpu().numpy(),
+                   logits=lgs[l].cpu().numpy())
+        _, _, flips = _check_layer(w, l, res)
+        assert flips == 0
+    del layers, g
+    torch.cuda.empty_cache()
 
 
 def test_argument_errors():

@@ -5,7 +5,8 @@ Same bars as the decode path: top-k indices bit-exact on identical f32
 logits; outputs and routing weights within 2e-3 relative L2 and max-abs <=
 1e-2 x RMS of the oracle output.  The tiny shapes are checked on every token;
 the full-size prefill workloads (512 tokens with hot experts, 4096 tokens
-with x50 outlier rows) on sampled tokens, plus properties of every token."""
+with x50 outlier rows) on every token as well, plus properties of every
+token."""
 import numpy as np
 import pytest
 
@@ -229,14 +230,6 @@ def test_wide_shapes_take_the_prefill_kernels_at_few_tokens(m):
 
 # ------------------------------------------------------ full-size prefill
 
-def _sample_tokens(w, res, n, must=()):
-    rng = np.random.default_rng(1234)
-    picks = set(int(t) for t in must)
-    picks |= set(int(t) for t in rng.choice(w.m, size=n, replace=False))
-    picks |= {0, w.m - 1}
-    return np.array(sorted(picks), dtype=np.int32)
-
-
 def _full_properties(w, layer, res):
     assert res["status"] == 0
     assert np.all(np.isfinite(res["out"]))
@@ -249,6 +242,7 @@ def _full_properties(w, layer, res):
 
 
 def test_prefill_m512_hot_full_shape():
+    """Every token of the 512-token hot-expert workload against the oracle."""
     w = W.WORKLOADS["prefill_m512_hot"]
     dl = stage_layer(w, 0, experts_on_gpu=True)
     res = gpu_forward(dl)
@@ -256,16 +250,21 @@ def test_prefill_m512_hot_full_shape():
     hot = W.hot_experts(w, 0)
     counts = np.bincount(res["topk_idx"].ravel(), minlength=w.n_routed)
     assert counts[hot].sum() > 0.5 * counts.sum()  # imbalanced routing
-    tokens = _sample_tokens(w, res, 24)
-    _check(w, 0, res, tokens=tokens)
+    _check(w, 0, res)
 
 
+@pytest.mark.slow
 def test_prefill_m4096_outliers_full_shape():
+    """Every token of the 4096-token workload with x50 outlier rows against
+    the oracle (a few minutes of oracle time on the host cores): every
+    (expert, row tile, column tile) of the call is compared, each expert's
+    last column tile included."""
     w = W.WORKLOADS["prefill_m4096_outliers"]
     dl = stage_layer(w, 0, experts_on_gpu=True)
     res = gpu_forward(dl)
     _full_properties(w, 0, res)
-    out_rows = W.outlier_rows(w, 0)
-    tokens = _sample_tokens(w, res, 16, must=out_rows[:8])
-    r = _check(w, 0, res, tokens=tokens)
+    r = _check(w, 0, res)
     assert r.clipped > 0
+    # the outlier rows on their own (their errors would vanish in the whole)
+    rows = W.outlier_rows(w, 0)
+    assert_close(res["out"][rows], r.out[rows], "outlier rows")

@@ -5,13 +5,15 @@ The streamed forward runs the same kernels as the resident forward on the
 same bytes (copied from a page-locked host arena into HBM slots), so its
 outputs must equal the resident forward's bit for bit; its cache counters
 must equal an independent model of the replacement policy fed with the
-same picks.  The router of moe_v41_route and the fused decode kernel's
+same picks; and every streamed output is checked against the oracle on the
+same inputs.  The router of moe_v41_route and the fused decode kernel's
 router share one accumulation order: their logits are compared bit for bit."""
 import numpy as np
 import pytest
 
+import oracle
 import synth.workloads as W
-from _helpers import lib_cfg
+from _helpers import assert_close, lib_cfg
 from test_cache_policy import ModelLRU
 
 pytestmark = pytest.mark.gpu
@@ -70,16 +72,27 @@ class Arena:
         self.copy_stream = torch.cuda.Stream()
 
 
-def _resident(cfg, dl, x, m):
+def _resident(cfg, dl, x, m, logits=None):
     w = dl.w
     ws = _ws(cfg)
     out = torch.empty((m, w.dim), dtype=torch.float32, device="cuda")
     tw = torch.empty((m, w.topk), dtype=torch.float32, device="cuda")
     ti = torch.empty((m, w.topk), dtype=torch.int32, device="cuda")
     Q.moe_v41_forward(cfg, x, m, dl.router_w, dl.bias, dl.expert_ptrs, w.shared_kind, dl.sh1, dl.sh3, dl.sh2, out,
-                      tw, ti, None, ws)
+                      tw, ti, logits, ws)
     assert Q.moe_v41_read_status(ws, clear=True) == 0
     return out, tw, ti
+
+
+def _oracle_check(w, layer, x_host, logits, out, tw, ti):
+    """The streamed call against the oracle: the layer's own seeded router,
+    bias, experts and shared expert, the step's x, the call's logits."""
+    experts = [W.expert_blocks(w, layer, e) for e in range(w.n_routed)]
+    r = oracle.moe_layer(oracle.cfg_of(w), x_host, W.router_bf16(w, layer), W.bias_f32(w, layer), experts,
+                         w.shared_kind, *W.shared_weights(w, layer), given_logits=logits)
+    np.testing.assert_array_equal(ti, r.topk_idx)
+    assert_close(tw, r.topk_w, "routing weights")
+    assert_close(out, r.out, "output")
 
 
 @pytest.mark.parametrize("m,prefetch_k,n_slots", [(1, 0, 2), (1, 2, 4), (1, 2, 9), (3, 0, 7), (20, 0, 16)])
@@ -97,6 +110,8 @@ def test_streamed_forward_equals_resident(m, prefetch_k, n_slots):
     host = torch.empty(m * w.topk + P, dtype=torch.int32, pin_memory=True)
     stream = torch.cuda.current_stream()
     xs = [stage_layer(w.with_(seed=w.seed + 100 + s), 0, experts_on_gpu=False).x for s in range(steps)]
+    xs_host = [W.x_bf16(w.with_(seed=w.seed + 100 + s), 0) for s in range(steps)]
+    lg = torch.empty((m, w.n_routed), dtype=torch.float32, device="cuda")
     for s in range(steps):
         x = xs[s]
         for l in range(layers):
@@ -110,10 +125,12 @@ def test_streamed_forward_equals_resident(m, prefetch_k, n_slots):
                                        w.shared_kind, dl.sh1, dl.sh3, dl.sh2, out, tw, ti, ws, host, stream,
                                        A.copy_stream)
             assert Q.moe_v41_read_status(ws, clear=True) == 0
-            ro, rw, ri = _resident(cfg, dl, x, m)
+            ro, rw, ri = _resident(cfg, dl, x, m, logits=lg)
             assert torch.equal(ti, ri)
             assert torch.equal(tw.view(torch.int32), rw.view(torch.int32))
             assert torch.equal(out.view(torch.int32), ro.view(torch.int32)), f"step {s} layer {l}"
+            _oracle_check(w, l, xs_host[s], lg.cpu().numpy(), out.cpu().numpy(), tw.cpu().numpy(),
+                          ti.cpu().numpy())
             picks = ti.cpu().numpy().reshape(-1)
             model.fetch(l, picks)
             if P and m == 1 and nxt is not None:

@@ -626,3 +626,37 @@ def test_parameter_accounting():
     assert w.w1_bytes // 84 * 256 == w.inter * w.dim
     assert w.w2_bytes // 110 * 256 == w.dim * w.inter
     assert w.expert_bytes == 12_810_240
+
+
+@pytest.mark.parametrize("variant", ["base", "kquant_shared", "topk1_no_norm", "no_clip_temp", "sigmoid",
+                                     "softmax", "image_tokens", "outliers", "ties"])
+def test_layer_equals_the_brute_force_dense_layer(variant):
+    """The factored oracle against its brute-force mode (every matrix
+    dequantised to dense f64 up front, textbook loops over all tokens, the
+    picks by k rounds of the best remaining key): equal to about 1e-12
+    relative, picks and weights identical."""
+    base = _tiny().with_(m=6)
+    w = {"base": base, "kquant_shared": base.with_(shared_kind=W.SHARED_KQUANT),
+         "topk1_no_norm": base.with_(topk=1, norm_topk_prob=False), "no_clip_temp": base.with_(
+             swiglu_limit=0.0, gate_temp=0.6, route_scale=2.0), "sigmoid": base.with_(score_func=1),
+         "softmax": base.with_(score_func=2), "image_tokens": base.with_(image_frac=0.5),
+         "outliers": base.with_(outlier_frac=0.34), "ties": base}[variant]
+    cfg = oracle.cfg_of(w)
+    L = _tiny_layer(w)
+    im = W.image_mask(w, 0)
+    bv = None if im is None else W.bias_vl_f32(w, 0)
+    gl = None
+    if variant == "ties":  # equal logits on most experts: the tie rule decides the picks
+        gl = np.full((w.m, w.n_routed), 0.25, dtype=np.float32)
+        gl[:, 5] = 0.3
+    a = oracle.moe_layer(cfg, L["x"], L["router_w"], L["bias"] * (0 if variant == "ties" else 1), L["experts"],
+                         w.shared_kind, *L["shared"], given_logits=gl, bias_vl=bv, image_mask=im)
+    b = oracle.moe_layer_dense(cfg, L["x"], L["router_w"], L["bias"] * (0 if variant == "ties" else 1),
+                               L["experts"], w.shared_kind, *L["shared"], given_logits=gl, bias_vl=bv,
+                               image_mask=im)
+    np.testing.assert_array_equal(a.topk_idx, b.topk_idx)
+    np.testing.assert_array_equal(a.topk_w, b.topk_w)
+    scale = np.abs(a.out).max()
+    np.testing.assert_allclose(b.out, a.out, rtol=1e-12, atol=1e-12 * scale)
+    if variant == "ties":
+        assert np.all(a.topk_idx[:, 0] == 5) and np.all(a.topk_idx[:, 1] == 0)

@@ -1,8 +1,10 @@
 """moe_v41_forward_noalloc: the forward for callers that cannot hand the
 library any device memory when they call (a plugin inside an engine that
 owns the whole GPU memory pool, a loop that must not call cudaMalloc).  Its
-scratch is a fixed array the library keeps on each GPU; the results must
-match moe_v41_forward's on the same inputs, call after call.
+scratch is a fixed array the library keeps on each GPU.  It runs the same
+deterministic decode kernel as moe_v41_forward, so its results must equal
+that call's bit for bit on the same inputs, call after call, and stay within
+the parity bars of the oracle.
 
 This file is collected last on purpose, and must pass both on its own in a
 fresh process and after every other test."""
@@ -10,7 +12,7 @@ import numpy as np
 import pytest
 
 import synth.workloads as W
-from _helpers import assert_close, gpu_forward, lib_cfg
+from _helpers import assert_close, gpu_forward, lib_cfg, oracle_for
 
 pytestmark = pytest.mark.gpu
 
@@ -45,8 +47,13 @@ def test_noalloc_matches_workspace_forward_twice(name, m):
         out, tw, ti, status = _noalloc(dl, cfg, m)
         assert status == 0
         np.testing.assert_array_equal(ti, ref["topk_idx"])
-        assert_close(tw, ref["topk_w"], "routing weights")
-        assert_close(out, ref["out"], "output")
+        np.testing.assert_array_equal(tw.view(np.int32), ref["topk_w"].view(np.int32))
+        np.testing.assert_array_equal(out.view(np.int32), ref["out"].view(np.int32))
+    # and the oracle, on the same logits
+    r = oracle_for(w, 0, given_logits=ref["logits"], picked=np.unique(ti))
+    np.testing.assert_array_equal(ti, r.topk_idx)
+    assert_close(tw, r.topk_w, "routing weights")
+    assert_close(out, r.out, "output")
 
 
 def test_noalloc_rejects_what_does_not_fit():
