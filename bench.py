@@ -57,11 +57,15 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=30)
     ap.add_argument("--prefill-m", type=int, default=0, help="tokens of the prefill call (default: the workload's)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 8-token decode and 512-token prefill lines")
     ap.add_argument("--no-streamed", action="store_true")
     ap.add_argument("--streamed-layers", type=int, default=4, help="layers of the host arena (streamed leg)")
     ap.add_argument("--streamed-slots", type=int, default=256, help="HBM expert slots of the streamed leg")
     ap.add_argument("--streamed-tokens", type=int, default=64, help="timed tokens of the streamed leg")
     ap.add_argument("--prefetch-k", type=int, default=6, help="predicted next-layer experts fetched ahead")
+    ap.add_argument("--mma-rates", action="store_true",
+                    help="only measure tcgen05.mma issue rates (kinds, widths, A in shared or tensor memory)")
     ap.add_argument("--graph", type=int, default=1,
                     help="1: time the decode step as one CUDA-graph replay of its layer calls; 0: eager launches")
     return ap.parse_args()
@@ -163,15 +167,67 @@ def recorded_traffic(workload: str):
 
 
 class Clocks:
-    """nvidia-smi samples during the timed region."""
+    """SM clock and clock-event reasons sampled every millisecond during the
+    timed region, through NVML (read-only queries; the GPU's settings are
+    never changed), else by nvidia-smi every 100 ms."""
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
     Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.thread = None
+        self.samples = []
+        self.max_mhz = None
+        self.nvml = None
+        self.handle = None
+
+    def _nvml_open(self):
+        import ctypes
+        try:
+            L = ctypes.CDLL("libnvidia-ml.so.1")
+            if L.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            bus = None
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(self.index)
+                bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+            except Exception:
+                bus = None
+            ok = bus is not None and L.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) == 0
+            if not ok and L.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) != 0:
+                return False
+            mx = ctypes.c_uint()
+            if L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.nvml, self.handle = L, h
+            return True
+        except (OSError, AttributeError):
+            return False
+
+    def _poll(self):
+        import ctypes
+        L, h = self.nvml, self.handle
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            L.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_flag:
+            if L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and get_reasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((float(mhz.value), int(rs.value)))
+            time.sleep(0.001)
 
     def start(self):
+        import threading
+        self.samples = []
+        self.stop_flag = False
+        if self._nvml_open():
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
@@ -180,6 +236,14 @@ class Clocks:
             self.proc = None
 
     def stop(self):
+        if self.thread is not None:
+            self.stop_flag = True
+            self.thread.join()
+            self.thread = None
+            sm = [m for m, _ in self.samples]
+            reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "samples": len(sm), "source": "nvml, 1 ms", "reasons": reasons}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -199,7 +263,7 @@ class Clocks:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "source": "nvidia-smi, 100 ms", "reasons": sorted(reasons)}
 
 
 # ----------------------------------------------------------- oracle (CPU)
@@ -222,9 +286,9 @@ def _oracle_run(w: W.Workload, inp, token: int):
 
 
 def cpu_baseline(w: W.Workload, layers_per_step: int, n_units: int, threads: int, target_s: float = 0.0):
-    """Time the oracle, as it stands, on (layer, token) units of the workload
-    spread over `threads` host threads: a fixed sample of distinct units
-    (tokens spread over the batch, layers over the step), repeated until the
+    """Time the oracle, as it stands, on a token sample of a one-layer
+    workload (the prefill calls): a fixed sample of distinct tokens spread
+    over the batch, run over `threads` host threads, repeated until the
     timed work reaches `target_s` seconds (or exactly n_units units when
     target_s is 0).  Returns (tokens/s, seconds, units, description)."""
     base = max(1, min(n_units, threads))
@@ -252,6 +316,60 @@ def cpu_baseline(w: W.Workload, layers_per_step: int, n_units: int, threads: int
     desc = (f"{n} (layer, token) units of {w.name} cycling over {base} distinct units ({len(layers)} layers, "
             f"tokens spread over the batch) on {threads} threads; tokens/s = units / layers per step / seconds")
     return tps, dt, n, desc
+
+
+class OracleSteps:
+    """The oracle, as it stands, timed on steps of a decode workload on the
+    host cores.  A full step is what the GPU step does: every token of the
+    call (m of them) through every layer of the step (L), i.e. m * L
+    (layer, token) units, submitted together to `threads` host threads and
+    waited for.  A bounded step takes the first `units` of those units (the
+    tokens of layer 0, then of layer 1, ...).  Used by the reference arm and
+    by the cpu_baseline of the decode lines, so both report the same thing."""
+
+    def __init__(self, w: W.Workload, L: int, threads: int):
+        self.w, self.L, self.threads = w, L, threads
+        self.full = [(l, t) for l in range(L) for t in range(w.m)]
+        with ThreadPoolExecutor(min(threads, 8)) as ex:
+            self.inputs = dict(zip(range(L), ex.map(lambda l: _oracle_inputs(w, l, list(range(w.m))), range(L))))
+        self.ex = ThreadPoolExecutor(threads)
+
+    def unit_seconds(self) -> float:
+        """wall time of one unit on one thread (calibration, not reported)"""
+        t0 = time.perf_counter()
+        _oracle_run(self.w, self.inputs[0], 0)
+        return time.perf_counter() - t0
+
+    def step(self, units: int) -> float:
+        todo = self.full[:units]
+        t0 = time.perf_counter()
+        list(self.ex.map(lambda u: _oracle_run(self.w, self.inputs[u[0]], u[1]), todo))
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.ex.shutdown()
+
+    def describe(self, units: int, steps: int) -> str:
+        full = len(self.full)
+        what = "a full step" if units == full else f"a bounded step: {units} of the {full}"
+        return (f"{steps} steps of {self.w.name}, each {what} (layer, token) units ({self.w.m} token(s) x "
+                f"{self.L} layers), submitted together to {self.threads} host threads and waited for; "
+                f"tokens/s = units / layers per step / seconds")
+
+
+def oracle_decode_baseline(w: W.Workload, L: int, threads: int, target_s: float):
+    """cpu_baseline of a decode line: whole steps until about target_s seconds."""
+    o = OracleSteps(w, L, threads)
+    try:
+        units = len(o.full)
+        o.step(units)  # warm-up and calibration
+        t1 = o.step(units)
+        n = max(1, int(round(target_s / max(t1, 1e-3))))
+        dt = sum(o.step(units) for _ in range(n))
+        tps = n * units / L / dt
+        return tps, dt, n, o.describe(units, n) + f", {dt:.1f} s"
+    finally:
+        o.close()
 
 
 # ------------------------------------------------------------------- GPU
@@ -417,18 +535,15 @@ def run_ours(args, rank, world, local_rank):
                 resident_experts=args.resident_experts)
 
 
-def run_prefill(args, local_rank):
-    """The long-prefill workload: one layer call of m tokens per step on the
-    prefill kernels, timed with events per call; then the same calls through
-    host buffers."""
+def run_call(args, local_rank, w: W.Workload, K: int):
+    """A one-layer workload (the prefill calls, the 8-token decode call): one
+    layer call of m tokens per step, timed with events per call; then the
+    same calls through host buffers."""
     import torch
     import quantized_mixture_experts_router_gb300 as Q
     from synth.device import stage_layer
 
     dev = torch.device("cuda", local_rank)
-    w = W.WORKLOADS[args.prefill_workload]
-    if args.prefill_m:
-        w = w.with_(m=args.prefill_m)
     d = stage_layer(w, 0, device=dev, experts_on_gpu=True, bulk_on_gpu=True, slots=args.resident_experts)
     cfg = Q.make_cfg(w.dim, w.inter, w.n_routed, w.topk, w.gate_temp, w.norm_topk_prob, w.route_scale,
                      w.swiglu_limit, max_tokens=w.m)
@@ -449,7 +564,6 @@ def run_prefill(args, local_rank):
     if st:
         raise RuntimeError(f"device status {st} during prefill warm-up")
     distinct = float(np.unique(ti.cpu().numpy()).size)
-    K = args.prefill_steps
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     torch.cuda.synchronize()
     clocks = Clocks(local_rank)
@@ -489,8 +603,10 @@ def run_prefill(args, local_rank):
     mean_ms, min_ms, e_ms = max_over_ranks([statistics.fmean(per_call), min(per_call), e2e["ms"] if e2e else 0.0], dev)
     if e2e:
         e2e["ms"] = e_ms
+    del d, ws, out, tw, ti
+    torch.cuda.empty_cache()
     return dict(w=w, K=K, per_call_ms=mean_ms, per_call_min_ms=min_ms, distinct=distinct,
-                clocks=clk, e2e=e2e, launches_per_call=launches)
+                clocks=clk, e2e=e2e, launches_per_call=launches, resident_experts=args.resident_experts)
 
 
 def _mem_available() -> int:
@@ -626,6 +742,43 @@ def stage_x(w, l, dev):
     return t
 
 
+def mma_rates(local_rank):
+    """tcgen05.mma throughput with every SM issuing back-to-back MMAs
+    (M = 128, one K step each) into one accumulator: f16, bf16 and e4m3
+    operands, widths 32..256, A from shared or from tensor memory.  Each
+    figure is the launch's CUDA-event time; TFLOP/s counts 2 * 128 * N * K
+    per MMA over all SMs.  (There is no int8 kind to measure: ptxas refuses
+    tcgen05.mma .kind::i8 for sm_103a.)"""
+    import ctypes
+    import torch
+    from quantized_mixture_experts_router_gb300.build import PEAKS_SO
+    torch.cuda.set_device(local_rank)
+    sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
+    L = ctypes.CDLL(PEAKS_SO)
+    L.mma_rate_run.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_float),
+                                                    ctypes.POINTER(ctypes.c_ulonglong)]
+    res = []
+    clocks = Clocks(local_rank)
+    clocks.start()
+    for kind, name, kdepth in ((0, "f16", 16), (1, "bf16", 16), (3, "e4m3", 32)):
+        for a_tmem in (0, 1):
+            for n in (32, 64, 128, 256):
+                iters = max(2000, 4000000 // n)
+                ms = ctypes.c_float()
+                clk = (ctypes.c_ulonglong * sms)()
+                rc = L.mma_rate_run(kind, n, a_tmem, iters, sms, ctypes.byref(ms), clk)
+                if rc != 0:
+                    res.append({"kind": name, "n": n, "a": "tmem" if a_tmem else "smem", "error": rc})
+                    continue
+                flops = 2.0 * 128 * n * kdepth * iters * sms
+                cyc = statistics.median(list(clk))
+                res.append({"kind": name, "n": n, "a": "tmem" if a_tmem else "smem", "iters": iters,
+                            "ms": ms.value, "tflops": flops / (ms.value / 1e3) / 1e12,
+                            "cycles_per_mma": cyc / iters, "macs_per_clk_sm": 128 * n * kdepth * iters / cyc})
+    clk = clocks.stop()
+    print(json.dumps({"mma_rates": res, "sms": sms, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -635,19 +788,35 @@ def main():
     L = args.layers or w.layers
     ncores = os.cpu_count() or 1
 
+    if args.mma_rates:
+        mma_rates(local_rank)
+        return
+
     if args.impl == "reference":
         # the CPU oracle as the reference arm: rank 0 only
         if rank != 0:
             return
         K, Wm = args.steps, args.warmup
-        cpu_baseline(w, L, max(1, min(Wm, ncores)), ncores)  # warm-up units
-        tps, dt, n, desc = cpu_baseline(w, L, K, ncores)
+        o = OracleSteps(w, L, ncores)
+        try:
+            unit_s = o.unit_seconds()
+            full = len(o.full)
+            # bounded steps when K + W full steps would not end within a few minutes
+            waves = int(150.0 / ((K + Wm) * max(unit_s, 1e-3)))
+            units = min(full, max(1, waves * ncores))
+            for _ in range(Wm):
+                o.step(units)
+            dt = sum(o.step(units) for _ in range(K))
+            desc = o.describe(units, K)
+        finally:
+            o.close()
+        tps = K * units / L / dt
         line = {"impl": "reference", "metric": metric_name(w), "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": K, "warmup": Wm, "ms_per_step": 1000.0 / tps, "higher_is_better": True,
+                "steps": K, "warmup": Wm, "ms_per_step": 1000.0 * dt / K, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": config_of(w, L, None),
+                "config": config_of(w, L),
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
-                                 "sample": f"each step one (layer, token) unit; {desc}"},
+                                 "sample": desc},
                 "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -656,10 +825,18 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     r = run_ours(args, rank, world, local_rank)
-    # the streamed leg runs before the prefill leg: after the prefill leg's end-to-end part its prefetch
-    # runs were up to 2.7x slower, an interaction of the legs, not part of either workload
+    # the streamed leg runs before the one-layer legs (see run_streamed)
     sm = None if (args.no_streamed or world > 1) else run_streamed(args, local_rank)
-    pf = None if args.no_prefill else run_prefill(args, local_rank)
+    calls = []
+    if not args.no_prefill:
+        pw = W.WORKLOADS[args.prefill_workload]
+        if args.prefill_m:
+            pw = pw.with_(m=args.prefill_m)
+        calls.append(("prefill", pw, args.prefill_steps))
+    if not args.no_extra:
+        calls.append(("prefill_m512", W.WORKLOADS["prefill_m512_hot"], args.prefill_steps))
+        calls.append(("decode_m8", W.WORKLOADS["decode_m8_kquant_shared"], max(args.prefill_steps, 30)))
+    res_calls = [(key, run_call(args, local_rank, cw, K)) for key, cw, K in calls]
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -672,7 +849,7 @@ def main():
         "metric": metric_name(w), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": r["ms"] / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8-dp4a/bf16-fma, f32 accumulate", "data": "synthetic",
-        "config": config_of(w, L, r),
+        "config": config_of(w, L), "run": run_of(r),
         "roofline": roofline(w, r["distinct"], r["per_call_ms"], r["kernel"], traffic),
         "gpu_launches": (r["launches_per_call"] or 0) * L * K,
         "clocks": r["clocks"],
@@ -682,30 +859,34 @@ def main():
         line["e2e"] = {"value": job_tokens_per_s(world, w.m, e["steps"], e["ms"]), "unit": "tokens/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
     if world == 1 and not args.no_cpu_baseline:
-        tps, dt, n, desc = cpu_baseline(w, L, ncores, ncores, target_s=12.0)
-        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
-                                "sample": desc + f", {dt:.1f} s"}
-    if pf:
+        tps, dt, n, desc = oracle_decode_baseline(w, L, ncores, 12.0)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle", "sample": desc}
+    for key, pf in res_calls:
         pw = pf["w"]
-        p = {"workload": pw.name, "metric": metric_name(pw), "value": job_tokens_per_s(world, pw.m, 1, pf["per_call_ms"]),
-             "unit": "tokens/s",
+        decode_like = pw.m <= 8
+        p = {"workload": pw.name, "metric": metric_name(pw),
+             "value": job_tokens_per_s(world, pw.m, 1, pf["per_call_ms"]), "unit": "tokens/s",
              "steps": pf["K"], "warmup": 3, "ms_per_step": pf["per_call_ms"], "ms_per_step_min": pf["per_call_min_ms"],
-             "config": config_of(pw, 1, {"distinct": pf["distinct"], "resident": 1, "rotated": False,
-                                         "resident_experts": args.resident_experts}),
+             "config": config_of(pw, 1), "run": run_of(pf),
              "roofline": roofline(pw, pf["distinct"], pf["per_call_ms"],
-                                  f"the prefill kernels of one layer call ({pf['launches_per_call']} launches)",
+                                  ("k_decode_layer (the whole layer call, one launch)" if pf["launches_per_call"] == 1
+                                   else f"the prefill kernels of one layer call ({pf['launches_per_call']} launches)"),
                                   recorded_traffic(pw.name)),
              "gpu_launches": pf["launches_per_call"] * pf["K"], "clocks": pf["clocks"],
-             "dtype": "fp16 tensor-core GEMMs (gate/up split hi+lo), bf16 router/shared, f32 accumulate"}
+             "dtype": ("int8-dp4a, f32 accumulate" if decode_like else
+                       "fp16 tensor-core GEMMs on exact-integer K-quant weights, bf16 router/shared, f32 accumulate")}
         if pf["e2e"]:
             e = pf["e2e"]
             p["e2e"] = {"value": job_tokens_per_s(world, pw.m, e["steps"], e["ms"]), "unit": "tokens/s",
                         "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
         if world == 1 and not args.no_cpu_baseline:
-            tps, dt, n, desc = cpu_baseline(pw, 1, ncores, ncores, target_s=10.0)
-            p["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
-                                 "sample": desc + f", {dt:.1f} s"}
-        line["prefill"] = p
+            if decode_like:
+                tps, dt, n, desc = oracle_decode_baseline(pw, 1, ncores, 6.0)
+            else:
+                tps, dt, n, desc = cpu_baseline(pw, 1, ncores, ncores, target_s=8.0)
+                desc += f", {dt:.1f} s"
+            p["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": ncores, "kind": "oracle", "sample": desc}
+        line[key] = p
     if sm:
         line["streamed"] = sm
     print(json.dumps(line), flush=True)
@@ -718,22 +899,27 @@ def metric_name(w: W.Workload) -> str:
     return f"MoE-layer tokens/s, {w.name} (m={w.m}, {w.layers} layer(s) per step)"
 
 
-def config_of(w: W.Workload, L: int, r):
-    c = {"workload": w.name, "dim": w.dim, "inter": w.inter, "n_routed": w.n_routed, "topk": w.topk, "m": w.m,
-         "layers_per_step": L, "shared": "bf16" if w.shared_kind == W.SHARED_BF16 else "Q2_K/Q3_K",
-         "experts": "Q2_K gate/up, Q3_K down, all resident in HBM",
-         "l2": "inputs larger than L2: each step streams every layer's weights (>6 GB) through the 129 MB L2"}
-    if r:
-        c["distinct_experts_per_call"] = r["distinct"]
-        c["resident_layers"] = r["resident"]
-        if "graph" in r:
-            c["launch"] = ("the step's layer calls captured once as a CUDA graph, replayed per step"
-                           if r["graph"] else "eager launches, one event per layer boundary")
-        if r.get("resident_experts"):
-            c["resident_experts"] = r["resident_experts"]
-            c["note_experts"] = "profiling run: expert e uses slot e % resident_experts"
-        if r["rotated"]:
-            c["note"] = "device memory held fewer layers than the step; layers rotate over the resident ones"
+def config_of(w: W.Workload, L: int):
+    """The workload the line measures (the same keys in both arms)."""
+    return {"workload": w.name, "dim": w.dim, "inter": w.inter, "n_routed": w.n_routed, "topk": w.topk, "m": w.m,
+            "layers_per_step": L, "shared": "bf16" if w.shared_kind == W.SHARED_BF16 else "Q2_K/Q3_K",
+            "experts": "Q2_K gate/up, Q3_K down, all resident in HBM",
+            "l2": ("inputs larger than L2: each step streams the step's expert weights "
+                   f"(>{algorithmic_bytes(w, min(w.n_routed, w.m * w.topk)) * L / 1e9:.1f} GB) through the "
+                   "129 MB L2")}
+
+
+def run_of(r):
+    """How this run executed the workload (our arm only)."""
+    c = {"distinct_experts_per_call": r["distinct"], "resident_layers": r.get("resident", 1)}
+    if "graph" in r:
+        c["launch"] = ("the step's layer calls captured once as a CUDA graph, replayed per step"
+                       if r["graph"] else "eager launches, one event per layer boundary")
+    if r.get("resident_experts"):
+        c["resident_experts"] = r["resident_experts"]
+        c["note_experts"] = "profiling run: expert e uses slot e % resident_experts"
+    if r.get("rotated"):
+        c["note"] = "device memory held fewer layers than the step; layers rotate over the resident ones"
     return c
 
 

@@ -11,6 +11,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 SO = os.path.join(OUT_DIR, "libmoe_v41.so")
+# measurement support, not part of the library: the tensor-core rate microbenchmark bench.py --mma-rates runs
+PEAKS_SRC = os.path.join(HERE, "peaks", "mma_rate.cu")
+PEAKS_SO = os.path.join(OUT_DIR, "libmma_rate.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -31,6 +34,8 @@ def build(verbose_ptxas: bool = False) -> str:
             cmd += ["-Xptxas", "-v"]
         objs.append(obj)
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+    peaks = [NVCC, *ARCH, *FLAGS, "-shared", PEAKS_SRC, "-o", PEAKS_SO]
+    procs.append((peaks, subprocess.Popen(peaks, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
     errs, logs = [], []
     for cmd, p in procs:
         out, _ = p.communicate()
