@@ -755,26 +755,30 @@ def mma_rates(local_rank):
     torch.cuda.set_device(local_rank)
     sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
     L = ctypes.CDLL(PEAKS_SO)
-    L.mma_rate_run.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_float),
+    L.mma_rate_run.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_float),
                                                     ctypes.POINTER(ctypes.c_ulonglong)]
     res = []
     clocks = Clocks(local_rank)
     clocks.start()
-    for kind, name, kdepth in ((0, "f16", 16), (1, "bf16", 16), (3, "e4m3", 32)):
-        for a_tmem in (0, 1):
-            for n in (32, 64, 128, 256):
-                iters = max(2000, 4000000 // n)
-                ms = ctypes.c_float()
-                clk = (ctypes.c_ulonglong * sms)()
-                rc = L.mma_rate_run(kind, n, a_tmem, iters, sms, ctypes.byref(ms), clk)
-                if rc != 0:
-                    res.append({"kind": name, "n": n, "a": "tmem" if a_tmem else "smem", "error": rc})
-                    continue
-                flops = 2.0 * 128 * n * kdepth * iters * sms
-                cyc = statistics.median(list(clk))
-                res.append({"kind": name, "n": n, "a": "tmem" if a_tmem else "smem", "iters": iters,
-                            "ms": ms.value, "tflops": flops / (ms.value / 1e3) / 1e12,
-                            "cycles_per_mma": cyc / iters, "macs_per_clk_sm": 128 * n * kdepth * iters / cyc})
+    cases = [(kind, name, kd, a, n, 128, 1) for kind, name, kd in ((0, "f16", 16), (1, "bf16", 16), (3, "e4m3", 32))
+             for a in (0, 1) for n in (32, 64, 128, 256)]
+    # independent accumulators cycled through, and the M = 64 shape
+    cases += [(0, "f16", 16, a, n, 128, nacc) for a in (0, 1) for n in (32, 64, 128) for nacc in (2, 4)
+              if nacc * n <= (256 if a else 512)]
+    cases += [(0, "f16", 16, 0, n, 64, nacc) for n in (64, 128, 256) for nacc in (1, 2) if nacc * n <= 512]
+    for kind, name, kdepth, a_tmem, n, mm, nacc in cases:
+        iters = max(2000, 4000000 // n) // 4 * 4
+        ms = ctypes.c_float()
+        clk = (ctypes.c_ulonglong * sms)()
+        rc = L.mma_rate_run(kind, n, mm, nacc, a_tmem, iters, sms, ctypes.byref(ms), clk)
+        tag = {"kind": name, "m": mm, "n": n, "nacc": nacc, "a": "tmem" if a_tmem else "smem"}
+        if rc != 0:
+            res.append(dict(tag, error=rc))
+            continue
+        flops = 2.0 * mm * n * kdepth * iters * sms
+        cyc = statistics.median(list(clk))
+        res.append(dict(tag, iters=iters, ms=ms.value, tflops=flops / (ms.value / 1e3) / 1e12,
+                        cycles_per_mma=cyc / iters, macs_per_clk_sm=mm * n * kdepth * iters / cyc))
     clk = clocks.stop()
     print(json.dumps({"mma_rates": res, "sms": sms, "clocks": clk}), flush=True)
 

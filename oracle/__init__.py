@@ -80,6 +80,9 @@ def lib():
         L.orc_moe_layer.restype = i32
         L.orc_moe_layer.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Layer), vp, i32, vp, vp, vp, i32,
                                     ctypes.POINTER(Stats)]
+        L.orc_flip_candidates.restype = i32
+        L.orc_flip_candidates.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Layer), i32, vp, vp, dbl, dbl, i32, vp,
+                                          vp]
         L.orc_moe_layer_dense.restype = i32
         L.orc_moe_layer_dense.argtypes = [ctypes.POINTER(Cfg), ctypes.POINTER(Layer), i32, vp, vp, vp]
         _lib = L
@@ -307,3 +310,45 @@ def moe_layer_dense(cfg: Cfg, x, router_w, bias, experts, shared_kind, sh1, sh3,
     if rc != 0:
         raise RuntimeError(f"dense oracle layer failed with status {rc}")
     return LayerResult(out, w, idx, 0, 0)
+
+
+@dataclass
+class Flips:
+    meta: np.ndarray       # i32 [n, 4]: slot (k = shared expert), kind, element or block, alternative
+    delta: np.ndarray      # f64 [n, dim]: the change each makes to the token's output
+    total: int             # candidates found (only the first max_c are held)
+
+
+FLIP_Q8_CODE, FLIP_Q8_SCALE, FLIP_BF16 = 0, 1, 2
+
+
+def flip_candidates(cfg: Cfg, x, t: int, topk_w, topk_idx, experts, shared_kind, sh1, sh3, sh2, kappa: float,
+                    min_change: float = 0.0, max_c: int = 4096) -> Flips:
+    """The requantisations of h that g and u known to within kappa * sum|terms|
+    can change, for token t of x routed to topk_idx with weights topk_w
+    (reading C-F1 of moe_oracle.c); those changing no output element by
+    min_change or more are left out."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    keep = []
+    table = (ctypes.c_void_p * (3 * cfg.n_routed))()
+    for e in range(cfg.n_routed):
+        ent = experts[e] if e < len(experts) else None
+        if ent is None:
+            continue
+        for j in range(3):
+            a = np.ascontiguousarray(ent[j], dtype=np.uint8)
+            keep.append(a)
+            table[3 * e + j] = a.ctypes.data
+    sh = [np.ascontiguousarray(s) for s in (sh1, sh3, sh2)]
+    L = Layer(_p(x), None, None, None, ctypes.cast(table, ctypes.c_void_p), shared_kind,
+              _p(sh[0]), _p(sh[1]), _p(sh[2]), None, None)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    meta = np.zeros((max_c, 4), dtype=np.int32)
+    delta = np.zeros((max_c, cfg.dim), dtype=np.float64)
+    n = lib().orc_flip_candidates(ctypes.byref(cfg), ctypes.byref(L), int(t), _p(w), _p(idx), float(kappa),
+                                  float(min_change), max_c, _p(meta), _p(delta))
+    if n < 0:
+        raise RuntimeError(f"oracle flip candidates failed with status {-n}")
+    k = min(n, max_c)
+    return Flips(meta[:k].copy(), delta[:k].copy(), n)

@@ -635,3 +635,265 @@ int orc_moe_layer_dense(const orc_cfg* c, const orc_layer* L, int m, double* out
   free(W1); free(W3); free(W2); free(S1); free(S3); free(S2); free(X); free(XQ); free(Z); free(G);
   return ORC_OK;
 }
+
+/* ------------------------------------------------- requantisation flips */
+
+/* Reading C-F1.  h is requantised twice in the method: to q8_1 before a
+ * K-quant down projection ([moe_v41.rs] swiglu_q8) and to bf16 before the
+ * bf16 shared expert's w2 ([MoE atlas] model.py Expert.forward).  Both are
+ * decisions taken on an f32 h, and an implementation that accumulates g and
+ * u in f32 holds them only to within some multiple of 2^-24 sum |terms|.
+ * Where the exact h lies that close to a rounding boundary, either side of
+ * the boundary is a result of the method.  orc_flip_candidates lists, for
+ * one token, each requantised value that a g' in [g - kappa sum|a x|,
+ * g + kappa sum|a x|] and a u' in the like interval of u can change, with
+ * the change it makes to the token's output:
+ *   kind 0  a q8_1 code of h (the block's scale as the oracle has it),
+ *   kind 1  a q8_1 block scale: the block's largest |h| moved far enough to
+ *           give another fp16(d); every code of the block taken again,
+ *   kind 2  a bf16 value of the bf16 shared expert's h.
+ * meta[4 c] = {slot (k: the shared expert), kind, element or block, the
+ * alternative code, fp16 bits of d, or bf16 bits}; delta[c D ..] = the
+ * output change (routing weight included; the shared expert's weight is 1).
+ * Candidates whose change stays below min_change in every output element
+ * are left out.  Returns the number of candidates; only the first max_c are
+ * written. */
+
+typedef struct {
+  int slot, kind, index, alt;
+  int j0, n;           /* output change: sum over i < n of coef[i] * W2[:, j0 + i] */
+  double coef[32];
+} flip_cand;
+
+typedef struct {
+  flip_cand* v;
+  int n, cap;
+} flip_list;
+
+static flip_cand* flip_push(flip_list* L) {
+  if (L->n == L->cap) {
+    L->cap = L->cap ? 2 * L->cap : 64;
+    L->v = (flip_cand*)realloc(L->v, sizeof(flip_cand) * (size_t)L->cap);
+  }
+  flip_cand* f = &L->v[L->n++];
+  memset(f, 0, sizeof(*f));
+  return f;
+}
+
+/* The smallest and largest swiglu over g' in [g - dg, g + dg], u' in
+ * [u - du, u + du]: for a fixed g' the value is linear in the clamped u', and
+ * for a fixed u' silu(min(g', limit)) has its one minimum at g*, the root
+ * of 1 + g (1 - sigma(g)) = 0 (the derivative of g sigma(g) over sigma(g)). */
+static void swiglu_range(double g, double u, double dg, double du, double limit, float* lo, float* hi) {
+  const double gstar = -1.2784645427610738;
+  double gs[3] = {g - dg, g + dg, gstar};
+  int ng = (gstar > g - dg && gstar < g + dg) ? 3 : 2;
+  double us[2] = {u - du, u + du};
+  float mn = 0.0f, mx = 0.0f;
+  int first = 1;
+  for (int a = 0; a < ng; ++a)
+    for (int b = 0; b < 2; ++b) {
+      float v = (float)orc_swiglu(gs[a], us[b], limit, NULL);
+      if (first || v < mn) mn = v;
+      if (first || v > mx) mx = v;
+      first = 0;
+    }
+  *lo = mn;
+  *hi = mx;
+}
+
+static int q8_code(float v, float d, float amax) {
+  int q = amax == 0.0f ? 0 : (int)round_half_away(v / d);
+  return q > 127 ? 127 : (q < -127 ? -127 : q);
+}
+
+/* The q8_1 candidates of one K-quant expert on one token (xh: q8_1(x) values). */
+static void flips_kquant(const orc_cfg* c, const double* xh, const uint8_t* w1, const uint8_t* w3, double G, int slot,
+                         double kappa, flip_list* F) {
+  int D = c->dim, I = c->inter;
+  double* row = (double*)malloc(sizeof(double) * D);
+  double* row3 = (double*)malloc(sizeof(double) * D);
+  float* h = (float*)malloc(sizeof(float) * I);
+  float* lo = (float*)malloc(sizeof(float) * I);
+  float* hi = (float*)malloc(sizeof(float) * I);
+  for (int r = 0; r < I; ++r) {
+    double g = 0.0, u = 0.0, sg = 0.0, su = 0.0;
+    dequant_row(2, w1, r, D, row);
+    dequant_row(2, w3, r, D, row3);
+    for (int d = 0; d < D; ++d) {
+      g += row[d] * xh[d];
+      u += row3[d] * xh[d];
+      sg += fabs(row[d] * xh[d]);
+      su += fabs(row3[d] * xh[d]);
+    }
+    h[r] = (float)orc_swiglu(g, u, c->swiglu_limit, NULL);
+    swiglu_range(g, u, kappa * sg, kappa * su, c->swiglu_limit, &lo[r], &hi[r]);
+  }
+  for (int b = 0; b < I / 32; ++b) {
+    const float* hb = h + 32 * b;
+    float amax = 0.0f, alo = 0.0f, ahi = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+      float a = fabsf(hb[i]);
+      if (a > amax) amax = a;
+      float l = lo[32 * b + i], u = hi[32 * b + i];
+      float mn = (l <= 0.0f && u >= 0.0f) ? 0.0f : fminf(fabsf(l), fabsf(u));
+      float mx = fmaxf(fabsf(l), fabsf(u));
+      if (mn > alo) alo = mn;
+      if (mx > ahi) ahi = mx;
+    }
+    const float d = (amax / 127.0f);  /* the q8_1 rule, reading C-L3 */
+    uint16_t d16 = orc_f16_from_f32(d);
+    double dv = orc_f16_value(d16);
+    int q[32];
+    for (int i = 0; i < 32; ++i) q[i] = q8_code(hb[i], d, amax);
+    for (int i = 0; i < 32; ++i) {
+      int qa = q8_code(lo[32 * b + i], d, amax), qb = q8_code(hi[32 * b + i], d, amax);
+      for (int qq = qa; qq <= qb; ++qq) {
+        if (qq == q[i]) continue;
+        flip_cand* f = flip_push(F);
+        f->slot = slot; f->kind = 0; f->index = 32 * b + i; f->alt = qq;
+        f->j0 = 32 * b + i; f->n = 1;
+        f->coef[0] = G * (double)(qq - q[i]) * dv;
+      }
+    }
+    float ends[2] = {alo, ahi};
+    uint16_t seen = d16;
+    for (int e = 0; e < 2; ++e) {
+      float d2 = ends[e] / 127.0f;
+      uint16_t b16 = orc_f16_from_f32(d2);
+      if (b16 == d16 || b16 == seen) continue;
+      seen = b16;
+      double dv2 = orc_f16_value(b16);
+      flip_cand* f = flip_push(F);
+      f->slot = slot; f->kind = 1; f->index = b; f->alt = b16;
+      f->j0 = 32 * b; f->n = 32;
+      int any = 0;
+      for (int i = 0; i < 32; ++i) {
+        int q2 = q8_code(hb[i], d2, ends[e]);
+        f->coef[i] = G * ((double)q2 * dv2 - (double)q[i] * dv);
+        any |= f->coef[i] != 0.0;
+      }
+      if (!any) --F->n;
+    }
+  }
+  free(row); free(row3); free(h); free(lo); free(hi);
+}
+
+/* bf16 bits as an integer in value order (-0 and +0 alike). */
+static int bf16_key(uint16_t b) { return (b & 0x8000u) ? -(int)(b & 0x7FFFu) : (int)b; }
+
+enum { BF16_SPAN = 16 };
+
+/* The bf16 candidates of the bf16 shared expert on one token. */
+static void flips_bf16(const orc_cfg* c, const uint16_t* x, const uint16_t* w1, const uint16_t* w3, int slot,
+                       double kappa, flip_list* F) {
+  int D = c->dim, I = c->inter;
+  for (int r = 0; r < I; ++r) {
+    double g = 0.0, u = 0.0, sg = 0.0, su = 0.0;
+    for (int d = 0; d < D; ++d) {
+      double xv = orc_bf16_value(x[d]);
+      double a = orc_bf16_value(w1[(size_t)r * D + d]) * xv, b = orc_bf16_value(w3[(size_t)r * D + d]) * xv;
+      g += a; u += b; sg += fabs(a); su += fabs(b);
+    }
+    float h = (float)orc_swiglu(g, u, c->swiglu_limit, NULL);
+    float lo, hi;
+    swiglu_range(g, u, kappa * sg, kappa * su, c->swiglu_limit, &lo, &hi);
+    /* every bf16 value between those of the window's ends (bf16 bits in
+     * value order: the sign-magnitude key); a window over more than
+     * BF16_SPAN values (h near 0) gives its two ends only */
+    uint16_t hb = orc_bf16_from_f32(h);
+    int k0 = bf16_key(orc_bf16_from_f32(lo)), k1 = bf16_key(orc_bf16_from_f32(hi)), kh = bf16_key(hb);
+    for (int key = k0; key <= k1; ++key) {
+      if (key == kh || (k1 - k0 > BF16_SPAN && key != k0 && key != k1)) continue;
+      uint16_t alt = key < 0 ? (uint16_t)(0x8000 | -key) : (uint16_t)key;
+      flip_cand* f = flip_push(F);
+      f->slot = slot; f->kind = 2; f->index = r; f->alt = alt;
+      f->j0 = r; f->n = 1;
+      f->coef[0] = orc_bf16_value(alt) - orc_bf16_value(hb);
+    }
+  }
+}
+
+/* Row d of an expert's W2 as f64 values. */
+static void w2_row(int kquant, const void* w2, int d, int I, double* row) {
+  if (kquant) dequant_row(3, (const uint8_t*)w2, d, I, row);
+  else
+    for (int j = 0; j < I; ++j) row[j] = orc_bf16_value(((const uint16_t*)w2)[(size_t)d * I + j]);
+}
+
+/* The change of one candidate in the output element whose W2 row is `row`. */
+static double flip_change(const flip_cand* f, const double* row) {
+  double s = 0.0;
+  for (int i = 0; i < f->n; ++i) s += f->coef[i] * row[f->j0 + i];
+  return s;
+}
+
+/* Candidates [from, F->n) of one expert: those whose output change reaches
+ * min_change in some element stay (the others are dropped from F), and the
+ * output changes of the ones among the first max_c overall are written.
+ * Two passes over the rows of W2: the largest change of each, then the
+ * changes. */
+static void flip_deltas(const orc_cfg* c, flip_list* F, int from, int max_c, int kquant, const void* w2,
+                        double min_change, double* delta) {
+  int D = c->dim, I = c->inter, n = F->n - from;
+  if (n <= 0) return;
+  double* row = (double*)malloc(sizeof(double) * I);
+  double* big = (double*)calloc((size_t)n, sizeof(double));
+  for (int d = 0; d < D; ++d) {
+    w2_row(kquant, w2, d, I, row);
+    for (int k = 0; k < n; ++k) {
+      double s = fabs(flip_change(&F->v[from + k], row));
+      if (s > big[k]) big[k] = s;
+    }
+  }
+  int kept = from;
+  for (int k = 0; k < n; ++k)
+    if (big[k] >= min_change && big[k] > 0.0) F->v[kept++] = F->v[from + k];
+  F->n = kept;
+  int to = F->n < max_c ? F->n : max_c;
+  if (from < to) {
+    for (int d = 0; d < D; ++d) {
+      w2_row(kquant, w2, d, I, row);
+      for (int k = from; k < to; ++k) delta[(size_t)k * D + d] = flip_change(&F->v[k], row);
+    }
+  }
+  free(row); free(big);
+}
+
+int orc_flip_candidates(const orc_cfg* c, const orc_layer* L, int t, const float* w, const int32_t* idx,
+                        double kappa, double min_change, int max_c, int32_t* meta, double* delta) {
+  int D = c->dim, k = c->topk;
+  const uint16_t* xt = L->x + (size_t)t * D;
+  float* xf = (float*)malloc(sizeof(float) * D);
+  uint8_t* xq8 = (uint8_t*)malloc((size_t)36 * (D / 32));
+  double* xh = (double*)malloc(sizeof(double) * D);
+  for (int d = 0; d < D; ++d) xf[d] = (float)orc_bf16_value(xt[d]);
+  orc_quantize_q8_1(xf, D, xq8);
+  orc_dequant_q8_1(xq8, D, xh);
+  flip_list F = {0};
+  int status = 0;
+  for (int s = 0; s <= k && !status; ++s) {
+    int from = F.n;
+    if (s < k) {
+      const uint8_t* const* ex = L->experts + 3 * idx[s];
+      if (!ex[0] || !ex[1] || !ex[2]) { status = -ORC_ERR_MISSING_EXPERT; break; }
+      flips_kquant(c, xh, ex[0], ex[1], (double)w[s], s, kappa, &F);
+      flip_deltas(c, &F, from, max_c, 1, ex[2], min_change, delta);
+    } else if (L->shared_kind == ORC_SHARED_KQUANT) {
+      flips_kquant(c, xh, (const uint8_t*)L->sh1, (const uint8_t*)L->sh3, 1.0, s, kappa, &F);
+      flip_deltas(c, &F, from, max_c, 1, L->sh2, min_change, delta);
+    } else {
+      flips_bf16(c, xt, (const uint16_t*)L->sh1, (const uint16_t*)L->sh3, s, kappa, &F);
+      flip_deltas(c, &F, from, max_c, 0, L->sh2, min_change, delta);
+    }
+  }
+  int n = status ? status : F.n;
+  for (int i = 0; i < F.n && i < max_c && !status; ++i) {
+    meta[4 * i + 0] = F.v[i].slot;
+    meta[4 * i + 1] = F.v[i].kind;
+    meta[4 * i + 2] = F.v[i].index;
+    meta[4 * i + 3] = F.v[i].alt;
+  }
+  free(F.v); free(xf); free(xq8); free(xh);
+  return n;
+}

@@ -63,6 +63,10 @@ void orc_expert_kquant(const orc_cfg* c, const uint8_t* xq8, const uint8_t* w1, 
                        const uint8_t* w2, double* E, int* clipped);
 void orc_shared_bf16(const orc_cfg* c, const uint16_t* x, const uint16_t* w1, const uint16_t* w3,
                      const uint16_t* w2, double* S, int* clipped);
+/* Requantisation alternatives of one token (reading C-F1 in moe_oracle.c):
+ * meta [max_c][4], delta [max_c][dim]; returns the count (or -status). */
+int orc_flip_candidates(const orc_cfg* c, const orc_layer* L, int t, const float* w, const int32_t* idx,
+                        double kappa, double min_change, int max_c, int32_t* meta, double* delta);
 int orc_moe_layer(const orc_cfg* c, const orc_layer* L, const int32_t* tokens, int n_tok, double* out,
                   float* topk_w, int32_t* topk_idx, int nthreads, orc_stats* stats);
 /* Brute-force mode for small inputs: dense f64 matrices up front, textbook

@@ -56,14 +56,15 @@ struct alignas(16) DecodePlan {
 // Prefill tiling: weight rows per GEMM tile, columns (pairs or tokens) per
 // tile, K values per pipeline stage, tokens per grouping chunk.
 constexpr int PF_TM = 128;
-constexpr int PF_TN = 256;     // down projection, router and shared-expert GEMMs
+constexpr int PF_TN = 256;     // router and bf16 shared-expert GEMMs
 constexpr int PF_TN_GU = 128;  // routed gate/up GEMM (hi/lo split operands)
 constexpr int PF_KC = 64;
 constexpr int PF_GCH = 64;
+constexpr int PF_TNQ = 64;     // routed down GEMM: pairs per tile (hi and lo parts stacked: an MMA of up to 128)
 
 // Byte offsets of the prefill regions, relative to the prefill base.
 struct PrefillLayout {
-  size_t xgh, xgl, chunk, offsets, expert_ok, pair_tok, pair_w, pos_of, pos_sh, n_tiles, gu_tiles, dn_tiles, h16,
+  size_t xgh, xgl, chunk, offsets, expert_ok, pair_tok, pair_w, pos_of, pos_sh, n_tiles, gu_tiles, dn_tiles, hh, hl,
       ep, hs, sp, total;
   size_t max_gu_tiles, max_dn_tiles;  // bounds on the column tiles over all experts
 };
@@ -86,8 +87,9 @@ inline PrefillLayout prefill_layout(const moe_v41_cfg& c) {
   const size_t T = (size_t)c.max_tokens, P = T * c.topk, V = P + T;  // pairs, plus the K-quant shared expert's
   const size_t NE = (size_t)c.n_routed + 1;
   const size_t nch = (T + PF_GCH - 1) / PF_GCH;
+  // an expert with n pairs takes ceil(n / tile width) column tiles
   L.max_gu_tiles = NE + V / PF_TN_GU + 1;
-  L.max_dn_tiles = NE + V / PF_TN + 1;
+  L.max_dn_tiles = NE + V / PF_TNQ + 1;
   L.xgh = take(V * c.dim * 2);
   L.xgl = take(V * c.dim * 2);
   L.chunk = take(nch * NE * 4);
@@ -98,9 +100,10 @@ inline PrefillLayout prefill_layout(const moe_v41_cfg& c) {
   L.pos_of = take(P * 4);
   L.pos_sh = take(T * 4);
   L.n_tiles = take(2 * 4);
-  L.gu_tiles = take(L.max_gu_tiles * (c.inter / PF_TM) * 16);
-  L.dn_tiles = take(L.max_dn_tiles * (c.dim / PF_TM) * 16);
-  L.h16 = take(V * c.inter * 2);
+  L.gu_tiles = take(L.max_gu_tiles * (c.inter / PF_TM) * 16);  // per tile: (e, mt, column tile, 0)
+  L.dn_tiles = take(L.max_dn_tiles * (c.dim / PF_TM) * 32);   // per tile: (e, mt, col0, ncol), W2 row-tile pointer
+  L.hh = take(V * c.inter * 2);
+  L.hl = take(V * c.inter * 2);
   L.ep = take(V * c.dim * 4);
   L.hs = take(T * c.inter * 2);
   L.sp = take(T * c.dim * 4);

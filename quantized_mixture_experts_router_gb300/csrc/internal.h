@@ -2,6 +2,8 @@
 // C-ABI file.
 #pragma once
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -101,6 +103,28 @@ inline int check_cfg(const moe_v41_cfg* c) {
   if (c->score_func < MOE_SCORE_SQRTSOFTPLUS || c->score_func > MOE_SCORE_SOFTMAX) return MOE_ERR_ARG;
   return MOE_OK;
 }
+
+// One launch of the persistent exact down GEMM of the routed experts (k_prefill_kq.cu).
+struct KqLaunch {
+  const void* bh;                       // q8_1(h) as fp16 hi / lo parts [b_rows][K]
+  const void* bl;
+  int b_rows;
+  const int4* tiles;                    // two int4 per tile: (expert, row tile, first pair, pairs <= PF_TNQ),
+                                        // the address of the tile's first W2 row
+  const int* n_tiles;                   // device count of tiles
+  int K, a_row_bytes, out_ld;
+  float* out_e;                         // E f32 [pair][out_ld]
+  unsigned* status;
+  unsigned long long timeout_ns;
+  unsigned grid;                        // persistent blocks (one per SM)
+};
+int launch_kq_gemm(const KqLaunch& L, cudaStream_t s);
+
+// A tensor map of a row-major matrix of 16-bit values [rows][cols] (cols a
+// multiple of 64, row pitch a multiple of 16 bytes), read in boxes of 64
+// values x box_rows rows into 128-byte-swizzled shared memory; rows past the
+// end read zeros.
+bool make_map_b16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows);
 
 int launch_quantize_q8_1(const void* x, int x_is_f32, int rows, int cols, void* q8, cudaStream_t s);
 int launch_select(const SelectParams& p, cudaStream_t s);

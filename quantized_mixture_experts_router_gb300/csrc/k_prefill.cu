@@ -14,11 +14,11 @@
 //           dequantised from Q2_K, split into high and low fp16 parts, times
 //           the pairs' xg rows (three products: hi.hi + hi.lo + lo.hi, about
 //           2^-22 relative); the epilogue applies the clipped SwiGLU,
-//           quantises h to q8_1 and stores fp16 of its values.  The split is
-//           needed because q8_1(h) turns any error in h near a rounding
-//           boundary into a whole quantisation step.
-//   down    W2 rows dequantised from Q3_K to fp16 times those h rows (one
-//           product; its rounding enters the output linearly) -> E per pair
+//           quantises h to q8_1 and stores its exact values as fp16 high +
+//           low parts.  The split is needed because q8_1(h) turns any error
+//           in h near a rounding boundary into a whole quantisation step.
+//   down    W2 (Q3_K) times those rows with exact products (the persistent
+//           GEMM of k_prefill_kq.cu) -> E per pair
 //   shared  bf16 shared expert: two bf16 GEMMs, h rounded to bf16 between them;
 //           a K-quant shared expert is one more expert taken by every token
 //   combine out = sum over the token's experts in ascending id of G_i E_i,
@@ -26,7 +26,7 @@
 //
 // GEMM block (128 weight rows x up to 128 or 256 columns): a TMA thread loads
 // the B rows (and bf16 A rows) of each K chunk into 128-byte-swizzled K-major
-// stage tiles; for K-quant A, sixteen producer warps dequantise staged raw
+// stage tiles; for Q2_K A, sixteen producer warps dequantise staged raw
 // blocks into the A tiles (four threads per weight row, one 16-value
 // sub-block each, through per-sub-block lookup tables); one thread issues
 // tcgen05.mma (M = 128, N = tile width, K = 16) into a tensor-memory
@@ -45,7 +45,7 @@ namespace {
 constexpr int TM = PF_TM;
 constexpr int KC = PF_KC;
 
-enum : int { A_BF16 = 0, A_Q2K = 1, A_Q3K = 2 };
+enum : int { A_BF16 = 0, A_Q2K = 1 };
 enum : int { E_F32 = 0, E_SWIGLU_Q8 = 1, E_SWIGLU_BF16 = 2 };
 
 __device__ __forceinline__ uint32_t f2h(float v) { return (uint32_t)__half_as_ushort(__float2half_rn(v)); }
@@ -152,9 +152,17 @@ __device__ __forceinline__ int block_scan_1024(int v, int* s32, int* total) {
 // One block of 1024 threads, two experts per thread: expert counts and
 // offsets, the chunk bases of the scatter (in place over the chunk counts),
 // which picked experts are usable, and the tile lists of both expert GEMMs.
+// Gate/up tiles are (expert, row tile, column tile of 128 pairs).  Down tiles
+// are two int4 each: (expert, row tile, first pair, pairs) and the address
+// of the tile's first W2 row (twice); an expert with n pairs takes ceil(n /
+// 64) of them with balanced widths (pairs [n t / c, n (t + 1) / c) for tile
+// t of c).  Row tiles are listed fastest, so that the row tiles of one
+// expert's pairs run side by side and share their activation rows in L2.
+// Expert N is the K-quant shared expert (its W2 is sh2).
 __global__ void __launch_bounds__(1024) k_group_scan(int* __restrict__ chunk, int nch, int N,
                                                      const unsigned long long* __restrict__ eptr, int gu_mt,
-                                                     int dn_mt, int* __restrict__ offsets, int* __restrict__ expert_ok,
+                                                     int dn_mt, size_t dn_row_tile, const uint8_t* sh2,
+                                                     int* __restrict__ offsets, int* __restrict__ expert_ok,
                                                      int4* __restrict__ gu_tiles, int4* __restrict__ dn_tiles,
                                                      int* __restrict__ n_tiles, unsigned* status) {
   __shared__ int s32[33];
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(1024) k_group_scan(int* __restrict__ chunk, in
         if (!ok[j]) atomicOr(status, (unsigned)MOE_STATUS_MISSING_EXPERT);
       }
       ng[j] = ok[j] ? (cnt[j] + PF_TN_GU - 1) / PF_TN_GU : 0;
-      nd[j] = ok[j] ? (cnt[j] + PF_TN - 1) / PF_TN : 0;
+      nd[j] = ok[j] ? (cnt[j] + PF_TNQ - 1) / PF_TNQ : 0;
     }
   }
   int total_pairs, total_g, total_d;
@@ -196,8 +204,18 @@ __global__ void __launch_bounds__(1024) k_group_scan(int* __restrict__ chunk, in
       }
       for (int t = 0; t < ng[j]; ++t)
         for (int mt = 0; mt < gu_mt; ++mt) gu_tiles[(size_t)(go + t) * gu_mt + mt] = make_int4(e, mt, t, 0);
-      for (int t = 0; t < nd[j]; ++t)
-        for (int mt = 0; mt < dn_mt; ++mt) dn_tiles[(size_t)(dof + t) * dn_mt + mt] = make_int4(e, mt, t, 0);
+      if (nd[j] > 0) {
+        const unsigned long long w2 = e == N ? reinterpret_cast<unsigned long long>(sh2) : __ldg(eptr + (size_t)e * 3 + 2);
+        for (int t = 0; t < nd[j]; ++t) {
+          const int a = (int)((long long)cnt[j] * t / nd[j]), b = (int)((long long)cnt[j] * (t + 1) / nd[j]);
+          for (int mt = 0; mt < dn_mt; ++mt) {
+            const unsigned long long rp = w2 + (unsigned long long)mt * dn_row_tile;
+            int4* d = dn_tiles + 2 * ((size_t)(dof + t) * dn_mt + mt);
+            d[0] = make_int4(e, mt, o + a, b - a);
+            d[1] = make_int4((int)(uint32_t)rp, (int)(uint32_t)(rp >> 32), (int)(uint32_t)rp, (int)(uint32_t)(rp >> 32));
+          }
+        }
+      }
     }
   }
   if (threadIdx.x == 0) {
@@ -311,13 +329,12 @@ __global__ void k_combine(const int* __restrict__ idx, const int* __restrict__ p
 }
 
 // ------------------------------------------------------------------ GEMM
-enum : int { B_TILED = 0, B_GATHER = 1 };
 constexpr int B_BOX = 16;  // rows per B box of the expert GEMMs: a tile loads only the rows it uses
 
 struct GemmArgs {
   CUtensorMap map_a[2];                // bf16 A matrices (box 64 x 128)
   CUtensorMap map_b[2];                // B rows (high, low parts): box 64 x B_BOX (expert jobs), 64 x TNM
-                                       // (plain jobs) or 64 x 1 (gather)
+                                       // (plain jobs)
   int K;                               // contraction length: a multiple of 256 (K-quant A) or 64 (bf16 A)
   int a_rows;                          // rows of A (the M extent)
   int a_row_bytes;                     // K-quant A: bytes per row
@@ -326,14 +343,14 @@ struct GemmArgs {
   const unsigned long long* eptr;      // expert jobs: the [N][3] pointer table
   int pj0, pj1;                        // pointer-table columns of the job's matrices
   int pseudo;                          // expert whose matrices are a0 / a1 (-1: none)
-  const int* b_rows;                   // gather: B row of each column
   int cols;                            // plain jobs: number of columns
   const int4* tiles;                   // expert jobs: (e, mt, nt) per block
   const int* n_tiles;
   const int* offsets;                  // expert jobs: column range of each expert
   int mt_count;                        // plain jobs: M tiles
   float* out_f32;                      // E_F32: out[col * ld + row]
-  uint16_t* out_h;                     // E_SWIGLU_*: h[col * ld + row]
+  uint16_t* out_h;                     // E_SWIGLU_*: h[col * ld + row] (E_SWIGLU_Q8: its high fp16 part)
+  uint16_t* out_h2;                    // E_SWIGLU_Q8: the low fp16 part
   int out_ld;
   float swiglu_limit;
   unsigned* status;
@@ -342,17 +359,16 @@ struct GemmArgs {
 
 constexpr uint32_t A_TILE = TM * 128;  // bytes of one A tile (128 rows x 64 values)
 
-// Raw K-quant staging.  A UNIT is the stretch of every tile row's blocks that
-// a group of consecutive K chunks reads: Q2_K half a super-block (2 chunks:
-// its 32 quant bytes, 8 scale bytes and d/dmin = 11 words), Q3_K a whole
-// super-block (4 chunks; the 4-byte-aligned window of 28 words over its 110
-// bytes, which are only 2-byte aligned).  Shared memory holds it row-major
-// with an odd pitch (11 or 29 words): the copies of one row's consecutive
-// words coalesce, and one word of 32 consecutive rows falls in 32 banks.
+// Raw Q2_K staging.  A UNIT is the stretch of every tile row's blocks that
+// a group of consecutive K chunks reads: half a super-block (2 chunks: its
+// 32 quant bytes, 8 scale bytes and d/dmin = 11 words).  Shared memory holds
+// it row-major with an odd pitch (11 words): the copies of one row's
+// consecutive words coalesce, and one word of 32 consecutive rows falls in 32
+// banks.
 template <int AK>
 struct RawGeo {
-  static constexpr int words() { return AK == A_Q2K ? 11 : 28; }
-  static constexpr int PITCH = AK == A_Q2K ? 11 : 29;
+  static constexpr int words() { return 11; }
+  static constexpr int PITCH = 11;
   static constexpr uint32_t BYTES = AK == A_BF16 ? 0u : (uint32_t)(TM * PITCH * 4);  // one matrix, one buffer
 };
 
@@ -395,7 +411,6 @@ struct Plan {
   }
 };
 
-constexpr int gcd_c(int a, int b) { return b == 0 ? a : gcd_c(b, a % b); }
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
@@ -440,16 +455,19 @@ __device__ __forceinline__ void q2k_tables(float d, float dmin, uint32_t scbyte,
 // same for q2, q3 (no byte carries into the next: 3 * 0x22 + 0x10 < 0x100).
 __device__ __forceinline__ uint32_t pair_sels(uint32_t qq) { return qq * 0x22u + 0x10101010u; }
 
-// q8_1 of one 32-value block of h held one value per lane: fp16 bits of
-// fp16(d) * q for this lane's value
-__device__ __forceinline__ uint16_t q8_h16_warp(float v) {
+// q8_1 of one 32-value block of h held one value per lane: the exact value
+// fp16(d) * q of this lane's element (11 x 7 significant bits) as fp16 high
+// and low parts whose sum is exact
+__device__ __forceinline__ void q8_hilo_warp(float v, uint16_t& hi, uint16_t& lo) {
   float amax = fabsf(v);
 #pragma unroll
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float d = __fdiv_rn(amax, 127.0f);
   const int q = amax == 0.0f ? 0 : q8_code(v, d, __frcp_rn(d));
-  const float dq = __half2float(__float2half_rn(d));
-  return (uint16_t)f2h(dq * (float)q);
+  const float x = __half2float(__float2half_rn(d)) * (float)q;
+  const __half h = __float2half_rn(x);
+  hi = __half_as_ushort(h);
+  lo = __half_as_ushort(__float2half_rn(x - __half2float(h)));
 }
 
 // One tile: D[128 rows, TN columns] (per matrix) = A . B^T over K.
@@ -466,7 +484,7 @@ __device__ __forceinline__ uint16_t q8_h16_warp(float v) {
 template <int AK>
 constexpr int loader_warps() { return AK == A_BF16 ? 0 : 4; }
 
-template <int AK, int NMAT, bool SPLIT, int EPI, int TNM, int NSA, int NSB, int RAWN, int NPROD, int BMODE>
+template <int AK, int NMAT, bool SPLIT, int EPI, int TNM, int NSA, int NSB, int RAWN, int NPROD>
 __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gemm(const __grid_constant__ GemmArgs g) {
   using PL = Plan<AK, NMAT, SPLIT, TNM, NSA, NSB, RAWN>;
   using RG = RawGeo<AK>;
@@ -478,7 +496,6 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
   extern __shared__ __align__(1024) uint8_t raw_smem[];
   uint8_t* sm = raw_smem + ((1024u - (smem_u32(raw_smem) & 1023u)) & 1023u);
   GemmCtl<NSA, NSB, RAWN>& C = *reinterpret_cast<GemmCtl<NSA, NSB, RAWN>*>(sm + PL::CTL);
-  int* s_rows = reinterpret_cast<int*>(sm + PL::ROWS);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int W_LOAD = NPW, W_TMA = NPW + NLW, W_MMA = NPW + NLW + 1;
   auto B = [](unsigned long long& b) { return reinterpret_cast<uint64_t*>(&b); };
@@ -543,9 +560,6 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
     }
     fence_mbar_init();
   }
-  if (BMODE == B_GATHER && warp == W_TMA) {
-    for (int i = lane; i < TN; i += 32) s_rows[i] = __ldg(g.b_rows + col0 + min(i, ncol - 1));
-  }
   if (warp == 0) tmem_alloc(&C.tmem, ncols_tmem);
   tc_fence_before();
   __syncthreads();
@@ -561,7 +575,7 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
       const bool row_ok = row0 + r < g.a_rows;
       const uint8_t* Am[2] = {A0, A1};
       const uint32_t raw_base = smem_u32(sm);
-      const int nunits = nk / (AK == A_Q2K ? 2 : 4);  // K chunks per unit: 2 (Q2_K half block), 4 (Q3_K block)
+      const int nunits = nk / 2;  // two K chunks per unit (half a Q2_K block)
       // this thread's 8 TMEM columns of A stage sa, matrix m, part pt: the
       // 16 K values 32 jj + 16 u .. + 15 of its row (lane = row)
       const uint32_t ta_lane = tmem + 256u + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(16 * jj + 8 * u);
@@ -653,68 +667,6 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
               }
             });
           }
-        } else {
-          // Q3_K super-block v: the row's 110 bytes start o = 0 or 2 bytes
-          // into the staged window; block word i = window bytes 4i+o .. 4i+o+3
-          static_assert(NMAT == 1 && !SPLIT, "the Q3_K producer serves the single-matrix, unsplit GEMM");
-          const uint32_t o = (uint32_t)(reinterpret_cast<uintptr_t>(Am[0] + (size_t)(row0 + r) * g.a_row_bytes +
-                                                                     (size_t)v * Q3K_B) & 3u);
-          const uint32_t fsel = o ? 0x5432u : 0x3210u;
-          const uint32_t* wv = rw[0];
-          uint32_t hm[4], sc[3], dword;
-          {
-            uint32_t prev = wv[(4 * u)];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {  // block words 4u .. 4u + 3 (hmask bytes 16u .. 16u + 15)
-              const uint32_t nxt = wv[(4 * u + i + 1)];
-              hm[i] = prmt(prev, nxt, fsel);
-              prev = nxt;
-            }
-            prev = wv[24];
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {  // block words 24 .. 26 (scales)
-              const uint32_t nxt = wv[(25 + i)];
-              sc[i] = prmt(prev, nxt, fsel);
-              prev = nxt;
-            }
-            dword = o ? (prev >> 16) : (prev & 0xFFFFu);  // block bytes 108, 109 (prev = window word 27)
-          }
-          const float d = half_bits_to_float(dword);
-          const __half2 m1028 = bits2h(0xE404E404u);  // -1028 in both halves
-#pragma unroll
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            uint32_t qs[4];
-            {
-              uint32_t prev = wv[(8 + 8 * hh + 4 * u)];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {  // block words 8 + 8hh + 4u + i (qs bytes 32hh + 16u + 4i ..)
-                const uint32_t nxt = wv[(9 + 8 * hh + 4 * u + i)];
-                qs[i] = prmt(prev, nxt, fsel);
-                prev = nxt;
-              }
-            }
-#pragma unroll
-            for (int cp = 0; cp < 2 && ok; ++cp) {
-              const int j = 2 * cp + jj;
-              ok = chunk(4 * v + 2 * hh + cp, [&](int sa) {
-                const int sbi = 2 * j + u;  // sub-block 8hh + sbi
-                const uint32_t lo4 = (sc[sbi >> 2] >> (8 * (sbi & 3) + 4 * hh)) & 15u;
-                const uint32_t hi2 = (sc[2] >> (8 * (sbi & 3) + 2 * (2 * hh + (j >> 1)))) & 3u;
-                const __half2 ds = __float2half2_rn(d * (float)((int)(lo4 | (hi2 << 4)) - 32));
-                uint32_t oh[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const uint32_t lo2 = (qs[i] >> (2 * j)) & 0x03030303u;
-                  const uint32_t hb = (hm[i] >> (4 * hh + j)) & 0x01010101u;
-                  const uint32_t q = lo2 + hb * 4u;  // lo | hb << 2, per byte: 0..7
-                  // fp16 1024 + q per value, minus 1028 (exact: q - 4), times d (code - 32)
-                  oh[2 * i] = h2bits(__hmul2(__hadd2(bits2h(prmt(q, 0x64646464u, 0x4140u)), m1028), ds));
-                  oh[2 * i + 1] = h2bits(__hmul2(__hadd2(bits2h(prmt(q, 0x64646464u, 0x4342u)), m1028), ds));
-                }
-                tmem_st8(ta_addr(sa, 0, 0), oh);
-              });
-            }
-          }
         }
         // raw buffer `buf` is free once every producer has read it
         mbar_arrive(B(C.raw_free[buf]));
@@ -756,7 +708,10 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
         } else {
           const float hv = swiglu_f32(v0[j], v1[j], g.swiglu_limit);
           if constexpr (EPI == E_SWIGLU_Q8) {
-            g.out_h[(size_t)(col0 + col) * g.out_ld + rw] = q8_h16_warp(hv);  // the warp's 32 rows: one q8_1 block
+            uint16_t hi, lo;
+            q8_hilo_warp(hv, hi, lo);  // the warp's 32 rows: one q8_1 block
+            g.out_h[(size_t)(col0 + col) * g.out_ld + rw] = hi;
+            g.out_h2[(size_t)(col0 + col) * g.out_ld + rw] = lo;
           } else {
             g.out_h[(size_t)(col0 + col) * g.out_ld + rw] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
           }
@@ -776,7 +731,7 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
       const int t = tid - W_LOAD * 32;
       const uint8_t* Am[2] = {A0, A1};
       const uint32_t raw_base = smem_u32(sm);
-      const int nunits = nk / (AK == A_Q2K ? 2 : 4);
+      const int nunits = nk / 2;
       const int lim = max(0, min(TM, g.a_rows - row0)) * WORDS;  // words of rows that exist
       const size_t rb = g.a_row_bytes;
       if constexpr (AK == A_Q2K) {
@@ -806,40 +761,6 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
           }
           cp_async_arrive(B(C.raw_full[buf]));  // once this thread's copies have landed
         }
-      } else {
-        // the words of a row start at its super-block's address rounded down
-        // to 4 bytes.  Copy j + P * q (P = WORDS / gcd(WORDS, NLT)) is copy j
-        // moved down by NLT * P / WORDS rows, so P offsets cover them all.
-        constexpr int P = WORDS / gcd_c(WORDS, NLT), NQ = TM * WORDS / (NLT * P), RQ = NLT * P / WORDS;
-        static_assert(TM * WORDS % (NLT * P) == 0, "whole periods per buffer");
-        uint32_t ro[P], wo[P], so[P];
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-          const int i = t + NLT * j, rr = i / WORDS, w = i - rr * WORDS;
-          ro[j] = (uint32_t)(rr * rb);
-          wo[j] = 4u * (uint32_t)w;
-          so[j] = 4u * (uint32_t)(rr * RG::PITCH + w);
-        }
-        for (int v = 0; v < nunits; ++v) {
-          const int buf = v % RAWN;
-          if (v >= RAWN && !mbar_wait_bounded(B(C.raw_free[buf]), (uint32_t)((v / RAWN - 1) & 1), deadline, g.status))
-            break;
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
-            const uintptr_t u0 = reinterpret_cast<uintptr_t>(Am[m] + (size_t)row0 * rb + (size_t)v * Q3K_B);
-            const uint32_t d0 = raw_base + PL::raw_off(m, buf);
-#pragma unroll 1
-            for (int q = 0; q < NQ; ++q) {
-              const uintptr_t u = u0 + (size_t)q * RQ * rb;
-              const uint32_t d = d0 + 4u * (uint32_t)(q * RQ * RG::PITCH);
-#pragma unroll
-              for (int j = 0; j < P; ++j)
-                if (t + NLT * (j + P * q) < lim)
-                  cp_async4(d + so[j], reinterpret_cast<const void*>(((u + ro[j]) & ~uintptr_t(3)) + wo[j]));
-            }
-          }
-          cp_async_arrive(B(C.raw_full[buf]));  // once this thread's copies have landed
-        }
       }
       // copies still in flight land before the block can exit
       asm volatile("cp.async.wait_all;" ::: "memory");
@@ -847,7 +768,7 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
   } else if (warp == W_TMA && lane == 0) {
     // ------------------------------------------------------- TMA issuer
     const bool boxed = g.tiles != nullptr;  // expert jobs: B_BOX-row boxes up to TN rows
-    const uint32_t bbytes = (uint32_t)(BMODE == B_GATHER || boxed ? TN : TNM) * 128u;
+    const uint32_t bbytes = (uint32_t)(boxed ? TN : TNM) * 128u;
     const uint32_t bytes = (KQ ? 0u : NMAT * A_TILE) + PL::NPART * bbytes;
     for (int kc = 0; kc < nk; ++kc) {
       const int sb = kc % NSB;
@@ -863,11 +784,7 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
       for (int pt = 0; pt < PL::NPART; ++pt) {
         const uint32_t dst = stack && pt == 1 ? smem_u32(sm + PL::b_off(sb, 0)) + (uint32_t)TN * 128u
                                               : smem_u32(sm + PL::b_off(sb, pt));
-        if constexpr (BMODE == B_GATHER) {
-          for (int i = 0; i < TN; i += 4)
-            tma_gather4(dst + (uint32_t)i * 128u, &g.map_b[pt], kc * KC, s_rows[i], s_rows[i + 1], s_rows[i + 2],
-                        s_rows[i + 3], fb);
-        } else if (boxed) {
+        if (boxed) {
           for (int i = 0; i < TN; i += B_BOX) tma_load_2d(dst + (uint32_t)i * 128u, &g.map_b[pt], kc * KC, col0 + i, fb);
         } else {
           tma_load_2d(dst, &g.map_b[pt], kc * KC, col0, fb);
@@ -927,11 +844,11 @@ __global__ void __launch_bounds__(NPROD + 32 * loader_warps<AK>() + 64, 1) k_gem
   }
 }
 
-template <int AK, int NMAT, bool SPLIT, int EPI, int TNM, int NSA, int NSB, int RAWN, int NPROD, int BMODE>
+template <int AK, int NMAT, bool SPLIT, int EPI, int TNM, int NSA, int NSB, int RAWN, int NPROD>
 int launch_gemm(const GemmArgs& g, unsigned grid, cudaStream_t s) {
   constexpr size_t smem = Plan<AK, NMAT, SPLIT, TNM, NSA, NSB, RAWN>::SMEM;
   static_assert(smem <= 232448, "GEMM stages exceed the shared memory of a block");
-  auto kern = k_gemm<AK, NMAT, SPLIT, EPI, TNM, NSA, NSB, RAWN, NPROD, BMODE>;
+  auto kern = k_gemm<AK, NMAT, SPLIT, EPI, TNM, NSA, NSB, RAWN, NPROD>;
   static int attr_dev = -1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -958,32 +875,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A row-major matrix of 16-bit values [rows][cols] (cols a multiple of 64,
-// row pitch a multiple of 16 bytes) read in boxes of 64 values x box_rows
-// rows into 128-byte-swizzled shared memory; rows past the end read zeros.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn || !base || rows == 0) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 constexpr int NP_KQ = 512;   // K-quant GEMMs: 16 dequantising warps
 constexpr int NP_BF = 128;   // bf16 GEMMs: 4 epilogue warps
 
 int route_steps(const PrefillParams& p, cudaStream_t s) {
   GemmArgs g{};
-  if (!make_map(&g.map_a[0], p.router_w, p.D, p.N, TM) || !make_map(&g.map_b[0], p.x, p.D, p.m, PF_TN))
+  if (!make_map_b16(&g.map_a[0], p.router_w, p.D, p.N, TM) || !make_map_b16(&g.map_b[0], p.x, p.D, p.m, PF_TN))
     return MOE_ERR_CUDA;
   g.K = p.D; g.a_rows = p.N; g.pseudo = -1; g.cols = p.m; g.mt_count = (p.N + TM - 1) / TM;
   g.out_f32 = p.logits; g.out_ld = p.N; g.status = &p.ctrl->status; g.timeout_ns = p.timeout_ns;
   const unsigned grid = (unsigned)(g.mt_count * ((p.m + PF_TN - 1) / PF_TN));
-  int rc = launch_gemm<A_BF16, 1, false, E_F32, PF_TN, 4, 4, 1, NP_BF, B_TILED>(g, grid, s);
+  int rc = launch_gemm<A_BF16, 1, false, E_F32, PF_TN, 4, 4, 1, NP_BF>(g, grid, s);
   if (rc) return rc;
   SelectParams sp{};
   sp.logits = p.logits; sp.bias = p.bias; sp.bias_vl = p.bias_vl; sp.image_mask = p.image_mask;
@@ -994,6 +896,18 @@ int route_steps(const PrefillParams& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool make_map_b16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base || rows == 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int launch_prefill_route(const PrefillParams& p, cudaStream_t s) { return route_steps(p, s); }
 
@@ -1018,7 +932,8 @@ int launch_prefill(const PrefillParams& p, cudaStream_t s) {
   int* n_tiles = reinterpret_cast<int*>(pw + L.n_tiles);
   int4* gu_tiles = reinterpret_cast<int4*>(pw + L.gu_tiles);
   int4* dn_tiles = reinterpret_cast<int4*>(pw + L.dn_tiles);
-  uint16_t* h16 = reinterpret_cast<uint16_t*>(pw + L.h16);
+  uint16_t* hh = reinterpret_cast<uint16_t*>(pw + L.hh);
+  uint16_t* hl = reinterpret_cast<uint16_t*>(pw + L.hl);
   float* ep = reinterpret_cast<float*>(pw + L.ep);
   uint16_t* hs = reinterpret_cast<uint16_t*>(pw + L.hs);
   float* sp = reinterpret_cast<float*>(pw + L.sp);
@@ -1027,8 +942,8 @@ int launch_prefill(const PrefillParams& p, cudaStream_t s) {
   if ((rc = route_steps(p, s))) return rc;
   // 3. grouping
   k_group_hist<<<nch, 256, NE * sizeof(int), s>>>(p.topk_idx, m, k, N, shq, chunk);
-  k_group_scan<<<1, 1024, 0, s>>>(chunk, nch, N, p.expert_ptrs, I / TM, D / TM, offsets, expert_ok, gu_tiles, dn_tiles,
-                                  n_tiles, &p.ctrl->status);
+  k_group_scan<<<1, 1024, 0, s>>>(chunk, nch, N, p.expert_ptrs, I / TM, D / TM, (size_t)TM * (I / QK) * Q3K_B,
+                                  p.sh2, offsets, expert_ok, gu_tiles, dn_tiles, n_tiles, &p.ctrl->status);
   k_group_scatter<<<nch, 256, 0, s>>>(p.topk_idx, p.topk_w, m, k, N, shq, chunk, pair_tok, pair_w, pos_of, pos_sh);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   // 4. the q8_1 values of x as fp16 high and low parts, in pair order
@@ -1039,47 +954,48 @@ int launch_prefill(const PrefillParams& p, cudaStream_t s) {
     k_xg<<<(unsigned)blocks, 256, 0, s>>>(p.x, m, D, k, pos_of, shq ? pos_sh : nullptr, xgh, xgl);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
-  // 5. gate/up of the routed experts (and of a K-quant shared expert) -> fp16 of q8_1(h)
+  // 5. gate/up of the routed experts (and of a K-quant shared expert) -> q8_1(h) as fp16 hi + lo
   {
     GemmArgs g{};
-    if (!make_map(&g.map_b[0], xgh, D, V, B_BOX) || !make_map(&g.map_b[1], xgl, D, V, B_BOX))
+    if (!make_map_b16(&g.map_b[0], xgh, D, V, B_BOX) || !make_map_b16(&g.map_b[1], xgl, D, V, B_BOX))
       return MOE_ERR_CUDA;
     g.K = D; g.a_rows = I; g.a_row_bytes = (D / QK) * Q2K_B; g.eptr = p.expert_ptrs; g.pj0 = 0; g.pj1 = 1;
     g.pseudo = shq ? N : -1; g.a0 = p.sh1; g.a1 = p.sh3;
-    g.tiles = gu_tiles; g.n_tiles = n_tiles; g.offsets = offsets; g.out_h = h16; g.out_ld = I;
+    g.tiles = gu_tiles; g.n_tiles = n_tiles; g.offsets = offsets; g.out_h = hh; g.out_h2 = hl; g.out_ld = I;
     g.swiglu_limit = p.swiglu_limit; g.status = &p.ctrl->status; g.timeout_ns = p.timeout_ns;
     const unsigned grid = (unsigned)L.max_gu_tiles * (unsigned)(I / TM);
-    if ((rc = launch_gemm<A_Q2K, 2, true, E_SWIGLU_Q8, PF_TN_GU, 2, 3, 3, NP_KQ, B_TILED>(g, grid, s))) return rc;
+    if ((rc = launch_gemm<A_Q2K, 2, true, E_SWIGLU_Q8, PF_TN_GU, 2, 3, 3, NP_KQ>(g, grid, s))) return rc;
   }
-  // 6. down -> E per pair
+  // 6. down -> E per pair (exact products, k_prefill_kq.cu)
   {
-    GemmArgs g{};
-    if (!make_map(&g.map_b[0], h16, I, V, B_BOX)) return MOE_ERR_CUDA;
-    g.K = I; g.a_rows = D; g.a_row_bytes = (I / QK) * Q3K_B; g.eptr = p.expert_ptrs; g.pj0 = 2; g.pj1 = 2;
-    g.pseudo = shq ? N : -1; g.a0 = p.sh2;
-    g.tiles = dn_tiles; g.n_tiles = n_tiles + 1; g.offsets = offsets; g.out_f32 = ep; g.out_ld = D;
-    g.status = &p.ctrl->status; g.timeout_ns = p.timeout_ns;
-    const unsigned grid = (unsigned)L.max_dn_tiles * (unsigned)(D / TM);
-    if ((rc = launch_gemm<A_Q3K, 1, false, E_F32, PF_TN, 4, 4, 4, NP_KQ, B_TILED>(g, grid, s))) return rc;
+    KqLaunch q{};
+    q.bh = hh; q.bl = hl; q.b_rows = V; q.tiles = dn_tiles; q.n_tiles = n_tiles + 1;
+    q.K = I; q.a_row_bytes = (I / QK) * Q3K_B; q.out_ld = D; q.out_e = ep;
+    q.status = &p.ctrl->status; q.timeout_ns = p.timeout_ns;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    q.grid = (unsigned)sms;
+    if ((rc = launch_kq_gemm(q, s))) return rc;
   }
   // 7. the bf16 shared expert
   if (!shq) {
     const unsigned ntok = (unsigned)((m + PF_TN - 1) / PF_TN);
     GemmArgs g{};
-    if (!make_map(&g.map_a[0], p.sh1, D, I, TM) || !make_map(&g.map_a[1], p.sh3, D, I, TM) ||
-        !make_map(&g.map_b[0], p.x, D, m, PF_TN))
+    if (!make_map_b16(&g.map_a[0], p.sh1, D, I, TM) || !make_map_b16(&g.map_a[1], p.sh3, D, I, TM) ||
+        !make_map_b16(&g.map_b[0], p.x, D, m, PF_TN))
       return MOE_ERR_CUDA;
     g.K = D; g.a_rows = I; g.pseudo = -1; g.cols = m;
     g.mt_count = I / TM; g.out_h = hs; g.out_ld = I; g.swiglu_limit = p.swiglu_limit;
     g.status = &p.ctrl->status; g.timeout_ns = p.timeout_ns;
-    if ((rc = launch_gemm<A_BF16, 2, false, E_SWIGLU_BF16, PF_TN, 3, 3, 1, NP_BF, B_TILED>(g, (unsigned)g.mt_count * ntok,
+    if ((rc = launch_gemm<A_BF16, 2, false, E_SWIGLU_BF16, PF_TN, 3, 3, 1, NP_BF>(g, (unsigned)g.mt_count * ntok,
                                                                                       s)))
       return rc;
     GemmArgs d{};
-    if (!make_map(&d.map_a[0], p.sh2, I, D, TM) || !make_map(&d.map_b[0], hs, I, m, PF_TN)) return MOE_ERR_CUDA;
+    if (!make_map_b16(&d.map_a[0], p.sh2, I, D, TM) || !make_map_b16(&d.map_b[0], hs, I, m, PF_TN)) return MOE_ERR_CUDA;
     d.K = I; d.a_rows = D; d.pseudo = -1; d.cols = m;
     d.mt_count = D / TM; d.out_f32 = sp; d.out_ld = D; d.status = &p.ctrl->status; d.timeout_ns = p.timeout_ns;
-    if ((rc = launch_gemm<A_BF16, 1, false, E_F32, PF_TN, 4, 4, 1, NP_BF, B_TILED>(d, (unsigned)d.mt_count * ntok, s)))
+    if ((rc = launch_gemm<A_BF16, 1, false, E_F32, PF_TN, 4, 4, 1, NP_BF>(d, (unsigned)d.mt_count * ntok, s)))
       return rc;
   }
   // 8. ordered combine

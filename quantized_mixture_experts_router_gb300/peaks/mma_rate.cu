@@ -29,10 +29,10 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
 
 // instruction descriptor: D format (bits 4-5), A / B formats (7-9, 10-12),
 // N >> 3 (17-22), M >> 4 (24-28); K-major operands
-__device__ __forceinline__ uint32_t idesc(int kind, int n) {
+__device__ __forceinline__ uint32_t idesc(int kind, int n, int m) {
   const uint32_t dfmt = 1u;                   // f32 accumulator
   const uint32_t ab = kind == 1 ? 1u : 0u;    // bf16 = 1; f16 and e4m3 = 0
-  return (dfmt << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  return (dfmt << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 template <int KIND, bool ATMEM>
@@ -66,7 +66,8 @@ constexpr int SMEM = 120 * 1024;
 static_assert(SMEM >= SMEM_USED, "operand tiles exceed the request");
 
 template <int KIND, bool ATMEM>
-__global__ void __launch_bounds__(128, 1) k_mma_rate(int n, int iters, unsigned long long* clk, unsigned* err) {
+__global__ void __launch_bounds__(128, 1) k_mma_rate(int n, int m, int nacc, int iters, unsigned long long* clk,
+                                                     unsigned* err) {
   extern __shared__ __align__(1024) uint8_t raw[];
   uint8_t* sm = raw + ((1024u - (su32(raw) & 1023u)) & 1023u);
   __shared__ uint32_t s_tmem;
@@ -88,13 +89,25 @@ __global__ void __launch_bounds__(128, 1) k_mma_rate(int n, int iters, unsigned 
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = s_tmem;
   if (tid == 0) {
-    const uint32_t id = idesc(KIND, n);
+    const uint32_t id = idesc(KIND, n, m);
     const uint32_t a0 = su32(sm), b0 = su32(sm + 128 * 128);
+    // everything an MMA needs is computed before the loop: the loop body is
+    // four MMA issues (K steps 0..3, accumulators cycled), so the issuing
+    // thread's own instructions do not set the rate
+    uint64_t ad[4], bd[4];
+    uint32_t dd[4], ta[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      ad[k] = sdesc(a0 + 32u * k);
+      bd[k] = sdesc(b0 + 32u * k);
+      ta[k] = tmem + 256u + 8u * k;
+      dd[k] = tmem + (uint32_t)((k % nacc) * n);
+    }
     const unsigned long long t0 = clock64();
 #pragma unroll 1
-    for (int i = 0; i < iters; ++i) {
-      const uint32_t k = (uint32_t)(i & 3);
-      mma<KIND, ATMEM>(tmem, sdesc(a0 + 32u * k), tmem + 256u + 8u * k, sdesc(b0 + 32u * k), id, i ? 1u : 0u);
+    for (int i = 0; i < iters; i += 4) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mma<KIND, ATMEM>(dd[k], ad[k], ta[k], bd[k], id, 1u);
     }
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(&bar))
                  : "memory");
@@ -114,7 +127,7 @@ __global__ void __launch_bounds__(128, 1) k_mma_rate(int n, int iters, unsigned 
 }
 
 template <int KIND, bool ATMEM>
-int run(int n, int iters, int blocks, float* ms, unsigned long long* clk_host) {
+int run(int n, int m, int nacc, int iters, int blocks, float* ms, unsigned long long* clk_host) {
   auto kern = k_mma_rate<KIND, ATMEM>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess) return 1;
   unsigned long long* clk = nullptr;
@@ -125,9 +138,9 @@ int run(int n, int iters, int blocks, float* ms, unsigned long long* clk_host) {
   cudaEvent_t e0, e1;
   cudaEventCreate(&e0);
   cudaEventCreate(&e1);
-  kern<<<blocks, 128, SMEM>>>(n, 64, clk, err);  // warm-up
+  kern<<<blocks, 128, SMEM>>>(n, m, nacc, 64, clk, err);  // warm-up
   cudaEventRecord(e0);
-  kern<<<blocks, 128, SMEM>>>(n, iters, clk, err);
+  kern<<<blocks, 128, SMEM>>>(n, m, nacc, iters, clk, err);
   cudaEventRecord(e1);
   int rc = cudaEventSynchronize(e1) == cudaSuccess ? 0 : 3;
   cudaEventElapsedTime(ms, e0, e1);
@@ -145,21 +158,27 @@ int run(int n, int iters, int blocks, float* ms, unsigned long long* clk_host) {
 
 }  // namespace
 
-// kind 0, 1 or 3 as above; n the MMA width (16..256, a multiple of 16); a_tmem: A read
-// from tensor memory; iters MMAs per block; blocks launched (one per SM).
+// kind 0, 1 or 3 as above; n the MMA width (16..256, a multiple of 16); m the
+// MMA height (64 or 128); nacc accumulators of n columns cycled through
+// (1, 2 or 4; nacc * n <= 256 with A in tensor memory, which starts at
+// column 256; <= 512 otherwise); a_tmem: A read from tensor memory; iters MMAs per block;
+// blocks launched (one per SM).
 // Writes the elapsed milliseconds and each block's issue-to-completion clock
 // cycles.  Returns 0 on success.
-extern "C" __attribute__((visibility("default"))) int mma_rate_run(int kind, int n, int a_tmem, int iters,
-                                                                  int blocks, float* ms,
+extern "C" __attribute__((visibility("default"))) int mma_rate_run(int kind, int n, int m, int nacc, int a_tmem,
+                                                                  int iters, int blocks, float* ms,
                                                                   unsigned long long* clk_per_block) {
   if (n < 16 || n > 256 || n % 16 || iters < 1 || blocks < 1) return -1;
+  if ((m != 64 && m != 128) || (nacc != 1 && nacc != 2 && nacc != 4) || nacc * n > (a_tmem ? 256 : 512)) return -1;
+  if (iters % 4) return -1;
+  if (m == 64 && n % 8) return -1;
   switch (kind * 2 + (a_tmem ? 1 : 0)) {
-    case 0: return run<0, false>(n, iters, blocks, ms, clk_per_block);
-    case 1: return run<0, true>(n, iters, blocks, ms, clk_per_block);
-    case 2: return run<1, false>(n, iters, blocks, ms, clk_per_block);
-    case 3: return run<1, true>(n, iters, blocks, ms, clk_per_block);
-    case 6: return run<3, false>(n, iters, blocks, ms, clk_per_block);
-    case 7: return run<3, true>(n, iters, blocks, ms, clk_per_block);
+    case 0: return run<0, false>(n, m, nacc, iters, blocks, ms, clk_per_block);
+    case 1: return run<0, true>(n, m, nacc, iters, blocks, ms, clk_per_block);
+    case 2: return run<1, false>(n, m, nacc, iters, blocks, ms, clk_per_block);
+    case 3: return run<1, true>(n, m, nacc, iters, blocks, ms, clk_per_block);
+    case 6: return run<3, false>(n, m, nacc, iters, blocks, ms, clk_per_block);
+    case 7: return run<3, true>(n, m, nacc, iters, blocks, ms, clk_per_block);
     default: return -1;
   }
 }

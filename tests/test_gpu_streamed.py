@@ -13,7 +13,7 @@ import pytest
 
 import oracle
 import synth.workloads as W
-from _helpers import assert_close, lib_cfg
+from _helpers import assert_close, assert_output, lib_cfg, oracle_run
 from test_cache_policy import ModelLRU
 
 pytestmark = pytest.mark.gpu
@@ -88,11 +88,11 @@ def _oracle_check(w, layer, x_host, logits, out, tw, ti):
     """The streamed call against the oracle: the layer's own seeded router,
     bias, experts and shared expert, the step's x, the call's logits."""
     experts = [W.expert_blocks(w, layer, e) for e in range(w.n_routed)]
-    r = oracle.moe_layer(oracle.cfg_of(w), x_host, W.router_bf16(w, layer), W.bias_f32(w, layer), experts,
-                         w.shared_kind, *W.shared_weights(w, layer), given_logits=logits)
+    r = oracle_run(oracle.cfg_of(w), x_host, W.router_bf16(w, layer), W.bias_f32(w, layer), experts,
+                   w.shared_kind, W.shared_weights(w, layer), given_logits=logits)
     np.testing.assert_array_equal(ti, r.topk_idx)
     assert_close(tw, r.topk_w, "routing weights")
-    assert_close(out, r.out, "output")
+    assert_output(out, r)
 
 
 @pytest.mark.parametrize("m,prefetch_k,n_slots", [(1, 0, 2), (1, 2, 4), (1, 2, 9), (3, 0, 7), (20, 0, 16)])

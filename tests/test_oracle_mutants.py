@@ -3,11 +3,13 @@
 Each mutant is the oracle's C source with one plausible error written in: a
 dropped term, a wrong sign, index or rounding rule, a transposed operand, a
 skipped step.  It is compiled into a library of its own, swapped in for the
-oracle, and at least one pin of test_oracle_pins.py has to fail on it: the
-pins hold the oracle to the pages and to mathematics, not only on its own
-happy path.  The unmodified source passes every pin (the control case).
+oracle, and at least one pin of test_oracle_pins.py or test_oracle_flips.py
+has to fail on it: the pins hold the oracle to the pages and to mathematics,
+not only on its own happy path.  The unmodified source passes every pin (the
+control case).
 """
 import inspect
+import itertools
 import os
 import subprocess
 
@@ -15,6 +17,7 @@ import pytest
 
 import oracle
 import oracle.build as ob
+import test_oracle_flips as flip_pins
 import test_oracle_pins as pins
 
 SRC = os.path.join(ob.HERE, "moe_oracle.c")
@@ -78,22 +81,39 @@ MUTANTS = [
     ("clamps_at_zero_limit", "if (limit > 0) {", "if (limit >= 0) {"),
     ("gate_and_up_swapped", "const uint8_t* w1 = L->experts[3 * e + 0];\n    const uint8_t* w3 = L->experts[3 * e + 1];",
      "const uint8_t* w1 = L->experts[3 * e + 1];\n    const uint8_t* w3 = L->experts[3 * e + 0];"),
+    # the requantisation flip candidates
+    ("flip_code_change_sign", "f->coef[0] = G * (double)(qq - q[i]) * dv;", "f->coef[0] = G * (double)(q[i] - qq) * dv;"),
+    ("flip_code_unscaled", "f->coef[0] = G * (double)(qq - q[i]) * dv;", "f->coef[0] = (double)(qq - q[i]) * dv;"),
+    ("flip_scale_keeps_codes", "int q2 = q8_code(hb[i], d2, ends[e]);", "int q2 = q[i];"),
+    ("flip_scale_one_column", "for (int i = 0; i < f->n; ++i) s += f->coef[i] * row[f->j0 + i];",
+     "for (int i = 0; i < f->n; ++i) s += f->coef[i] * row[f->j0];"),
+    ("flip_window_on_gate_only", "swiglu_range(g, u, kappa * sg, kappa * su, c->swiglu_limit, &lo[r], &hi[r]);",
+     "swiglu_range(g, u, kappa * sg, 0.0, c->swiglu_limit, &lo[r], &hi[r]);"),
+    ("flip_bf16_ends_only", "if (key == kh || (k1 - k0 > BF16_SPAN && key != k0 && key != k1)) continue;",
+     "if (key == kh || (key != k0 && key != k1)) continue;"),
+    ("flip_bf16_change_from_zero", "f->coef[0] = orc_bf16_value(alt) - orc_bf16_value(hb);",
+     "f->coef[0] = orc_bf16_value(alt);"),
 ]
 
 
 def _pin_cases():
-    """Every pin of test_oracle_pins.py with each of its parameter sets."""
-    for name, fn in inspect.getmembers(pins, inspect.isfunction):
-        if not name.startswith("test_") or fn.__module__ != pins.__name__:
-            continue
-        marks = [mk for mk in getattr(fn, "pytestmark", []) if mk.name == "parametrize"]
-        if not marks:
-            yield name, fn, {}
-            continue
-        argnames, values = marks[0].args[:2]
-        names = [a.strip() for a in argnames.split(",")] if isinstance(argnames, str) else list(argnames)
-        for v in values:
-            yield name, fn, dict(zip(names, v if len(names) > 1 else (v,)))
+    """Every pin of the two pin modules with each of its parameter sets."""
+    for mod in (pins, flip_pins):
+        for name, fn in inspect.getmembers(mod, inspect.isfunction):
+            if not name.startswith("test_") or fn.__module__ != mod.__name__:
+                continue
+            sets = []
+            for mk in getattr(fn, "pytestmark", []):
+                if mk.name != "parametrize":
+                    continue
+                argnames, values = mk.args[:2]
+                names = [a.strip() for a in argnames.split(",")] if isinstance(argnames, str) else list(argnames)
+                sets.append([dict(zip(names, v if len(names) > 1 else (v,))) for v in values])
+            for combo in itertools.product(*sets):
+                kw = {}
+                for d in combo:
+                    kw.update(d)
+                yield name, fn, kw
 
 
 def _first_failing_pin():

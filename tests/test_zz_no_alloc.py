@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import synth.workloads as W
-from _helpers import assert_close, gpu_forward, lib_cfg, oracle_for
+from _helpers import assert_close, assert_output, gpu_forward, lib_cfg, oracle_for
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +53,7 @@ def test_noalloc_matches_workspace_forward_twice(name, m):
     r = oracle_for(w, 0, given_logits=ref["logits"], picked=np.unique(ti))
     np.testing.assert_array_equal(ti, r.topk_idx)
     assert_close(tw, r.topk_w, "routing weights")
-    assert_close(out, r.out, "output")
+    assert_output(out, r)
 
 
 def test_noalloc_rejects_what_does_not_fit():
