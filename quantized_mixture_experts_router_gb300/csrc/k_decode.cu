@@ -778,6 +778,10 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     if (lane == 0) mbar_arrive(bar(C.pbar));
   } else if (warp == W_PROD) {
     // ---------------------------------------------------------- producer
+    // Lane 0 takes the tickets and picks the next item; the lanes then issue
+    // the item's stages in parallel (lane l: stages l, l + 32, ... of the
+    // item), each waiting only for its own ring slot, so that the ticket and
+    // item logic is paid once per item rather than once per stage.
     if (lane == 0) {
       // x and the expert pointer table are inputs of the call: copy them to
       // shared memory at once
@@ -794,179 +798,210 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
         mbar_arrive_expect_tx(bar(C.cbar[CB_BIAS]), (uint32_t)(p.N * 4));
         bulk_g2s(smem_base() + p.sm_bias, p.bias, (uint32_t)(p.N * 4), bar(C.cbar[CB_BIAS]));
       }
-      uint32_t n = 0;  // stages issued
-      uint32_t j = 0;  // items started
-      int n_exp = -1;
-      bool ok = true;
-      bool local_done = false;
-      const int rb = (p.D / QK) * Q2K_B, rb2 = (p.I / QK) * Q3K_B;
-      unsigned* const ctr[N_STREAMS] = {&p.ctrl->ticket, &p.ctrl->ticket_sh, &p.ctrl->ticket_gu, &p.ctrl->ticket_dn};
-      bool exhausted[N_STREAMS] = {false, false, false, false};
-      const DecodePlan* splan = reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan);
-      // the stream to take the next ticket from: -1 nothing left, N_STREAMS
-      // wait for the plan first
-      // Before the plan exists, shared down items are taken only once the
-      // shared h is complete: their tasks would otherwise hold ring stages
-      // while they wait, and the routed gate/up items could not get in.
-      bool sh_ready = false;
-      auto shared_ready = [&]() -> bool {
-        if (!sh_ready) sh_ready = ld_acquire(&p.ctrl->shgu_done) >= (unsigned)z.n_shgu;
-        return sh_ready;
-      };
-      auto choose = [&]() -> int {
-        if (!exhausted[S_MAIN]) return S_MAIN;
-        if (n_exp < 0 && mbar_try_wait(bar(C.pbar), 0u)) n_exp = splan->n_exp;
-        if (n_exp >= 0 && !exhausted[S_GU]) return S_GU;
-        if (!exhausted[S_SHDN] && (n_exp >= 0 || shared_ready())) return S_SHDN;
-        if (n_exp < 0) return N_STREAMS;
-        return exhausted[S_DN] ? -1 : S_DN;
-      };
-      // one ticket is taken ahead, so that its atomic is in flight while
-      // the current item streams
-      int ps = -1;
-      unsigned pt = 0;
-      for (;;) {
-        if (ps < 0) {
-          const int sel = choose();
-          if (sel < 0) break;
-          if (sel == N_STREAMS) {
-            // wait for the plan, or for the shared h while shared down items are left
-            uint32_t spins = 0;
-            for (;;) {
-              if (mbar_try_wait(bar(C.pbar), 0u)) {
-                n_exp = splan->n_exp;
-                break;
-              }
-              if (!exhausted[S_SHDN] && shared_ready()) break;
-              __nanosleep(200);
-              if ((++spins & 15u) == 0 && globaltimer_ns() > deadline) {
-                atomicOr(&p.ctrl->status, (unsigned)MOE_STATUS_TIMEOUT);
-                ok = false;
-                break;
-              }
-            }
-            if (!ok) break;
-            continue;
-          }
-          ps = sel;
-          pt = atomicAdd(ctr[sel], 1u);
-        }
-        Item it = decode_ticket(ps, pt, z, groups, n_exp);
-        if (it.kind == -2) {
-          exhausted[ps] = true;
-          ps = -1;
-          continue;
-        }
-        // the block-local item goes in before the block's first item past the router rows
-        if (!local_done && it.kind != I_Q8 && it.kind != I_ROUTER) {
-          local_done = true;
-          it = Item{I_LOCAL, 0, 0, 0, 0};  // the ticket stays taken for the next round
-        } else {
-          const int sel = choose();
-          ps = (sel >= 0 && sel < N_STREAMS) ? sel : -1;
-          if (ps >= 0) pt = atomicAdd(ctr[ps], 1u);
-        }
-        int ns;
-        switch (it.kind) {
-          case I_Q8: ns = 1; break;
-          case I_ROUTER: ns = 1; break;
-          case I_SHGU_B: ns = 2 * min(SHP, p.I - it.a * SHP); break;
-          case I_GU: ns = GT / GR; break;
-          case I_SHDN: ns = z.dn_sh_parts; break;
-          case I_LOCAL: ns = NCW; break;
-          default: ns = n_exp; break;
-        }
-        const uint32_t islot = j % NIS;
-        if (j >= (uint32_t)NIS &&
-            !(ok = mbar_wait_bounded(bar(C.item_done[islot]), (j / NIS - 1) & 1u, deadline, &p.ctrl->status)))
-          break;
-        it.remaining = (unsigned)ns;
-        C.item[islot] = it;
-        for (int s = 0; s < ns; ++s) {
-          const uint32_t slot = n % NST, use = n / NST;
-          if (use > 0 && !(ok = mbar_wait_bounded(bar(C.empty[slot]), (use - 1) & 1u, deadline, &p.ctrl->status)))
-            break;
-          Hdr h{K_STOP, (int)islot, 0, 0, n};
-          const uint8_t *a = nullptr, *b = nullptr;
-          uint32_t bytes = 0, boff = 0;
-          switch (it.kind) {
-            case I_Q8:
-              h.kind = K_Q8; h.a = it.a;
-              break;
-            case I_LOCAL:
-              h.kind = K_LOCAL; h.a = s;
-              break;
-            case I_ROUTER: {
-              const int r0 = it.a * RR;
-              h.kind = K_ROUTER; h.a = r0;
-              a = reinterpret_cast<const uint8_t*>(p.router_w) + (size_t)r0 * 2 * p.D;
-              bytes = (uint32_t)(min(RR, p.N - r0) * 2 * p.D);
-              break;
-            }
-            case I_SHGU_B: {
-              const int row = it.a * SHP + s / 2;
-              h.kind = K_SHGU_B; h.a = s / 2; h.b = s & 1;
-              a = ((s & 1) ? p.sh3 : p.sh1) + (size_t)row * 2 * p.D;
-              bytes = (uint32_t)(2 * p.D);
-              break;
-            }
-            case I_GU: {
-              const int r0 = it.b * GT + s * GR;
-              h.kind = K_GU_Q; h.a = it.a; h.b = s;
-              const uint8_t *w1, *w3;
-              if (it.a < 0) {
-                w1 = p.sh1; w3 = p.sh3;
-              } else {
-                const DecodePlan* sp = reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan);
-                w1 = reinterpret_cast<const uint8_t*>(sp->exp_ptr[it.a][0]);
-                w3 = reinterpret_cast<const uint8_t*>(sp->exp_ptr[it.a][1]);
-              }
-              if (w1 && w3) {
-                a = w1 + (size_t)r0 * rb;
-                b = w3 + (size_t)r0 * rb;
-                bytes = (uint32_t)(GR * rb);
-                boff = bytes;
-              }
-              break;
-            }
-            case I_SHDN: {  // the shared expert's rows of the group
-              const int d0 = it.a * DG;
-              if (z.shq) {
-                h.kind = K_DN_SHQ;
-                a = p.sh2 + (size_t)d0 * rb2;
-                bytes = (uint32_t)(DG * rb2);
-              } else {
-                h.kind = K_DN_SHB; h.a = s;
-                a = p.sh2 + (size_t)(d0 + s * SDR) * 2 * p.I;
-                bytes = (uint32_t)(SDR * 2 * p.I);
-              }
-              break;
-            }
-            default: {  // I_DN: the experts in ascending id
-              const int d0 = it.a * DG;
-              {
-                const int e = s;
-                h.kind = K_DN_RT; h.a = e;
-                const unsigned long long w2 =
-                    reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan)->exp_ptr[e][2];
-                if (w2) {
-                  a = reinterpret_cast<const uint8_t*>(w2) + (size_t)d0 * rb2;
-                  bytes = (uint32_t)(DG * rb2);
+    }
+    uint32_t n = 0;  // stages issued
+    uint32_t j = 0;  // items started
+    bool ok = true;
+    const int rb = (p.D / QK) * Q2K_B, rb2 = (p.I / QK) * Q3K_B;
+    const DecodePlan* splan = reinterpret_cast<const DecodePlan*>(smem_base() + p.sm_plan);
+    // ticket state, used by lane 0 only
+    int n_exp = -1;
+    bool local_done = false;
+    unsigned* const ctr[N_STREAMS] = {&p.ctrl->ticket, &p.ctrl->ticket_sh, &p.ctrl->ticket_gu, &p.ctrl->ticket_dn};
+    bool exhausted[N_STREAMS] = {false, false, false, false};
+    // the stream to take the next ticket from: -1 nothing left, N_STREAMS
+    // wait for the plan first
+    // Before the plan exists, shared down items are taken only once the
+    // shared h is complete: their tasks would otherwise hold ring stages
+    // while they wait, and the routed gate/up items could not get in.
+    bool sh_ready = false;
+    auto shared_ready = [&]() -> bool {
+      if (!sh_ready) sh_ready = ld_acquire(&p.ctrl->shgu_done) >= (unsigned)z.n_shgu;
+      return sh_ready;
+    };
+    auto choose = [&]() -> int {
+      if (!exhausted[S_MAIN]) return S_MAIN;
+      if (n_exp < 0 && mbar_try_wait(bar(C.pbar), 0u)) n_exp = splan->n_exp;
+      if (n_exp >= 0 && !exhausted[S_GU]) return S_GU;
+      if (!exhausted[S_SHDN] && (n_exp >= 0 || shared_ready())) return S_SHDN;
+      if (n_exp < 0) return N_STREAMS;
+      return exhausted[S_DN] ? -1 : S_DN;
+    };
+    // one ticket is taken ahead, so that its atomic is in flight while
+    // the current item streams
+    int ps = -1;
+    unsigned pt = 0;
+    for (;;) {
+      // --- lane 0: the next item (kind -1: none left, -3: stop on an error)
+      Item it{-1, 0, 0, 0, 0};
+      int ns = 0;
+      if (lane == 0) {
+        for (;;) {
+          if (ps < 0) {
+            const int sel = choose();
+            if (sel < 0) break;
+            if (sel == N_STREAMS) {
+              // wait for the plan, or for the shared h while shared down items are left
+              uint32_t spins = 0;
+              for (;;) {
+                if (mbar_try_wait(bar(C.pbar), 0u)) {
+                  n_exp = splan->n_exp;
+                  break;
+                }
+                if (!exhausted[S_SHDN] && shared_ready()) break;
+                __nanosleep(200);
+                if ((++spins & 15u) == 0 && globaltimer_ns() > deadline) {
+                  atomicOr(&p.ctrl->status, (unsigned)MOE_STATUS_TIMEOUT);
+                  it.kind = -3;
+                  break;
                 }
               }
-              break;
+              if (it.kind == -3) break;
+              continue;
             }
+            ps = sel;
+            pt = atomicAdd(ctr[sel], 1u);
           }
-          C.hdr[slot] = h;
-          uint8_t* dst = smem_base() + (size_t)slot * SB;
-          mbar_arrive_expect_tx(bar(C.full[slot]), a ? (b ? 2u * bytes : bytes) : 0u);
-          if (a) bulk_g2s(dst, a, bytes, bar(C.full[slot]));
-          if (a && b) bulk_g2s(dst + boff, b, bytes, bar(C.full[slot]));
-          ++n;
+          Item t = decode_ticket(ps, pt, z, groups, n_exp);
+          if (t.kind == -2) {
+            exhausted[ps] = true;
+            ps = -1;
+            continue;
+          }
+          // the block-local item goes in before the block's first item past the router rows
+          if (!local_done && t.kind != I_Q8 && t.kind != I_ROUTER) {
+            local_done = true;
+            t = Item{I_LOCAL, 0, 0, 0, 0};  // the ticket stays taken for the next round
+          } else {
+            const int sel = choose();
+            ps = (sel >= 0 && sel < N_STREAMS) ? sel : -1;
+            if (ps >= 0) pt = atomicAdd(ctr[ps], 1u);
+          }
+          it = t;
+          break;
         }
-        if (!ok) break;
-        ++j;
+        if (it.kind >= 0) {
+          switch (it.kind) {
+            case I_Q8: ns = 1; break;
+            case I_ROUTER: ns = 1; break;
+            case I_SHGU_B: ns = 2 * min(SHP, p.I - it.a * SHP); break;
+            case I_GU: ns = GT / GR; break;
+            case I_SHDN: ns = z.dn_sh_parts; break;
+            case I_LOCAL: ns = NCW; break;
+            default: ns = n_exp; break;
+          }
+          const uint32_t islot = j % NIS;
+          if (j >= (uint32_t)NIS &&
+              !mbar_wait_bounded(bar(C.item_done[islot]), (j / NIS - 1) & 1u, deadline, &p.ctrl->status)) {
+            it.kind = -3;
+          } else {
+            it.remaining = (unsigned)ns;
+            C.item[islot] = it;
+          }
+        }
       }
+      it.kind = __shfl_sync(0xffffffffu, it.kind, 0);
+      if (it.kind < 0) {
+        ok = it.kind != -3;
+        break;
+      }
+      it.a = __shfl_sync(0xffffffffu, it.a, 0);
+      it.b = __shfl_sync(0xffffffffu, it.b, 0);
+      ns = __shfl_sync(0xffffffffu, ns, 0);
+      __syncwarp();  // the item state (lane 0) before any of its stages
+      // --- the lanes: the item's stages, in rounds of at most NST (one per
+      // ring slot).  A round starts once the previous one is issued, so the
+      // empty barrier a lane waits on is at most one phase behind the use
+      // it waits for (its parity alone then identifies that use).
+      const uint32_t islot = j % NIS;
+      bool lane_ok = true;
+      for (int base = 0; base < ns; base += NST) {
+        __syncwarp();
+        const int s = base + lane;
+        if (lane >= NST || s >= ns || !lane_ok) continue;
+        const uint32_t sn = n + (uint32_t)s, slot = sn % NST, use = sn / NST;
+        if (use > 0 && !mbar_wait_bounded(bar(C.empty[slot]), (use - 1) & 1u, deadline, &p.ctrl->status)) {
+          lane_ok = false;
+          continue;
+        }
+        Hdr h{K_STOP, (int)islot, 0, 0, sn};
+        const uint8_t *a = nullptr, *b = nullptr;
+        uint32_t bytes = 0, boff = 0;
+        switch (it.kind) {
+          case I_Q8:
+            h.kind = K_Q8; h.a = it.a;
+            break;
+          case I_LOCAL:
+            h.kind = K_LOCAL; h.a = s;
+            break;
+          case I_ROUTER: {
+            const int r0 = it.a * RR;
+            h.kind = K_ROUTER; h.a = r0;
+            a = reinterpret_cast<const uint8_t*>(p.router_w) + (size_t)r0 * 2 * p.D;
+            bytes = (uint32_t)(min(RR, p.N - r0) * 2 * p.D);
+            break;
+          }
+          case I_SHGU_B: {
+            const int row = it.a * SHP + s / 2;
+            h.kind = K_SHGU_B; h.a = s / 2; h.b = s & 1;
+            a = ((s & 1) ? p.sh3 : p.sh1) + (size_t)row * 2 * p.D;
+            bytes = (uint32_t)(2 * p.D);
+            break;
+          }
+          case I_GU: {
+            const int r0 = it.b * GT + s * GR;
+            h.kind = K_GU_Q; h.a = it.a; h.b = s;
+            const uint8_t *w1, *w3;
+            if (it.a < 0) {
+              w1 = p.sh1; w3 = p.sh3;
+            } else {
+              w1 = reinterpret_cast<const uint8_t*>(splan->exp_ptr[it.a][0]);
+              w3 = reinterpret_cast<const uint8_t*>(splan->exp_ptr[it.a][1]);
+            }
+            if (w1 && w3) {
+              a = w1 + (size_t)r0 * rb;
+              b = w3 + (size_t)r0 * rb;
+              bytes = (uint32_t)(GR * rb);
+              boff = bytes;
+            }
+            break;
+          }
+          case I_SHDN: {  // the shared expert's rows of the group
+            const int d0 = it.a * DG;
+            if (z.shq) {
+              h.kind = K_DN_SHQ;
+              a = p.sh2 + (size_t)d0 * rb2;
+              bytes = (uint32_t)(DG * rb2);
+            } else {
+              h.kind = K_DN_SHB; h.a = s;
+              a = p.sh2 + (size_t)(d0 + s * SDR) * 2 * p.I;
+              bytes = (uint32_t)(SDR * 2 * p.I);
+            }
+            break;
+          }
+          default: {  // I_DN: expert s of the plan (ascending id), the group's rows
+            const int d0 = it.a * DG;
+            h.kind = K_DN_RT; h.a = s;
+            const unsigned long long w2 = splan->exp_ptr[s][2];
+            if (w2) {
+              a = reinterpret_cast<const uint8_t*>(w2) + (size_t)d0 * rb2;
+              bytes = (uint32_t)(DG * rb2);
+            }
+            break;
+          }
+        }
+        C.hdr[slot] = h;
+        uint8_t* dst = smem_base() + (size_t)slot * SB;
+        mbar_arrive_expect_tx(bar(C.full[slot]), a ? (b ? 2u * bytes : bytes) : 0u);
+        if (a) bulk_g2s(dst, a, bytes, bar(C.full[slot]));
+        if (a && b) bulk_g2s(dst + boff, b, bytes, bar(C.full[slot]));
+      }
+      ok = __all_sync(0xffffffffu, lane_ok);
+      n += (uint32_t)ns;
+      if (!ok) break;
+      ++j;
+    }
+    if (lane == 0) {
       if (ok) {
         // one stop per consumer warp
         for (int s = 0; s < NCW; ++s) {
