@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--streamed-slots", type=int, default=256, help="HBM expert slots of the streamed leg")
     ap.add_argument("--streamed-tokens", type=int, default=64, help="timed tokens of the streamed leg")
     ap.add_argument("--prefetch-k", type=int, default=6, help="predicted next-layer experts fetched ahead")
+    ap.add_argument("--streamed-reps", type=int, default=2, help="repetitions of each streamed configuration")
+    ap.add_argument("--streamed-only", action="store_true",
+                    help="run only the streamed leg and print its JSON object (the main run starts it this way)")
     ap.add_argument("--mma-rates", action="store_true",
                     help="only measure tcgen05.mma issue rates (kinds, widths, A in shared or tensor memory)")
     ap.add_argument("--graph", type=int, default=1,
@@ -132,7 +135,7 @@ def roofline(w: W.Workload, distinct: float, per_call_ms: float, kernel: str, tr
 
 KERNEL_SOURCES = {
     "decode": ["k_decode.cu", "select.cuh", "common.cuh", "internal.h"],
-    "prefill": ["k_prefill.cu", "tc.cuh", "k_route.cu", "select.cuh", "common.cuh", "internal.h"],
+    "prefill": ["k_prefill.cu", "k_prefill_kq.cu", "tc.cuh", "k_route.cu", "select.cuh", "common.cuh", "internal.h"],
 }
 
 
@@ -619,6 +622,30 @@ def _mem_available() -> int:
     return 0
 
 
+def streamed_in_child(args):
+    """The streamed leg in a process of its own.  In the process that ran the
+    other legs its timings depended on them (same box, same code): after the
+    e2e leg the prefetch runs took 1.2-1.3 ms per layer call instead of 0.39,
+    after the prefill leg single runs took up to 1.0 ms instead of 0.47; alone,
+    or after the CPU baseline, three repetitions agreed within 2%."""
+    import gc
+
+    import torch
+    gc.collect()
+    torch.cuda.empty_cache()  # the child needs the device memory the earlier legs held
+    cmd = [sys.executable, os.path.abspath(__file__), "--streamed-only", "--workload", args.workload,
+           "--warmup", str(args.warmup), "--streamed-layers", str(args.streamed_layers),
+           "--streamed-slots", str(args.streamed_slots), "--streamed-tokens", str(args.streamed_tokens),
+           "--prefetch-k", str(args.prefetch_k), "--streamed-reps", str(args.streamed_reps)]
+    p = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+    if p.returncode != 0:
+        return {"skipped": "streamed leg failed: " + (p.stderr.strip().splitlines() or ["?"])[-1]}
+    lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+    sm = json.loads(lines[-1]) if lines else {"skipped": "streamed leg printed no result"}
+    sm["process"] = "a child process of its own (its timings depended on the legs run before it in one process)"
+    return sm
+
+
 def run_streamed(args, local_rank):
     """The decode workload with the routed experts streamed: every expert of
     a few layers in a page-locked host arena, a least-recently-used set of HBM
@@ -680,7 +707,8 @@ def run_streamed(args, local_rank):
         copy_stream = torch.cuda.Stream(device=dev)
         runs = []
         # each configuration twice, alternating: repetitions on one box have differed by up to 2.7x
-        plan_runs = [(rep, P) for rep in range(2) for P in ([0, args.prefetch_k] if args.prefetch_k > 0 else [0])]
+        plan_runs = [(rep, P) for rep in range(args.streamed_reps)
+                     for P in ([0, args.prefetch_k] if args.prefetch_k > 0 else [0])]
         for rep, P in plan_runs:
             slots = torch.empty((S, slot), dtype=torch.uint8, device=dev)
             tables = torch.empty((Ls, w.n_routed, 3), dtype=torch.int64, device=dev)
@@ -795,6 +823,9 @@ def main():
     if args.mma_rates:
         mma_rates(local_rank)
         return
+    if args.streamed_only:
+        print(json.dumps(run_streamed(args, local_rank)), flush=True)
+        return
 
     if args.impl == "reference":
         # the CPU oracle as the reference arm: rank 0 only
@@ -829,8 +860,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     r = run_ours(args, rank, world, local_rank)
-    # the streamed leg runs before the one-layer legs (see run_streamed)
-    sm = None if (args.no_streamed or world > 1) else run_streamed(args, local_rank)
+    sm = None if (args.no_streamed or world > 1) else streamed_in_child(args)
     calls = []
     if not args.no_prefill:
         pw = W.WORKLOADS[args.prefill_workload]
