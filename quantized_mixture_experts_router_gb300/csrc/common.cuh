@@ -60,7 +60,7 @@ constexpr int PF_TN = 256;     // router and bf16 shared-expert GEMMs
 constexpr int PF_TN_GU = 128;  // routed gate/up GEMM (hi/lo split operands)
 constexpr int PF_KC = 64;
 constexpr int PF_GCH = 64;
-constexpr int PF_TNQ = 64;     // routed down GEMM: pairs per tile (hi and lo parts stacked: an MMA of up to 128)
+constexpr int PF_TNQ = 128;    // routed down GEMM: pairs per tile (hi and lo parts stacked: an MMA of up to 256)
 
 // Byte offsets of the prefill regions, relative to the prefill base.
 struct PrefillLayout {

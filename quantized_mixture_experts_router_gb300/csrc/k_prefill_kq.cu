@@ -1,20 +1,23 @@
 // Prefill path, the down projection: E = W2 q8_1(h) per (expert, token) pair
 // (Q3_K weights), as a persistent tcgen05 kernel over (expert, 128 rows of
-// W2, <= 64 pairs) tiles with exact products.
+// W2, <= 128 pairs) tiles with exact products.
 //
-//   A  the weights' integer part (code - 32) * q, q in -4..3, exact in fp16;
-//      the per-super-block factor d (fp16) is left out of A.
+//   A  the weights' integer part (code - 32) * q, q in -4..3, exact in fp16,
+//      written by the dequantising warps into a 128-byte-swizzled K-major
+//      shared-memory tile per 64-value chunk; the per-super-block factor d
+//      (fp16) is left out of A.
 //   B  the q8_1 values of h, fp16(d_h) * q_h (18 significant bits), as the two
 //      fp16 parts hi + lo whose sum is exact (written so by the gate/up
-//      epilogue); the parts are stacked as the first and second 64 rows of
-//      one B tile, so one MMA of width 64 + n forms A*hi and A*lo for n pairs.
+//      epilogue); the tile's n pairs' hi rows and then their lo rows form one
+//      B tile of 2n rows, so one MMA of width 2n forms A*hi and A*lo.
 // Each super-block (256 K values) accumulates into a fresh tensor-memory
-// accumulator, two of them alternating; the epilogue warps drain each, add
-// the hi and lo halves and scale by the super-block's d into f32 running
-// sums in registers while the MMAs of the next super-block proceed.  The
-// only rounding is the f32 accumulation, so an error that every clipped
-// element of a row of h shares (they all hold the block maximum) cannot add
-// up coherently along the row.
+// accumulator, two of them alternating (2 x 256 columns: all of tensor
+// memory); the epilogue warps drain each, add the hi and lo halves and scale
+// by the super-block's d into f32 running sums in registers while the MMAs of
+// the next super-block proceed.  The only rounding is the f32 accumulation,
+// so an error that every clipped element of a row of h shares (they all hold
+// the block maximum) cannot add up coherently along the row.  An expert with
+// up to 128 pairs dequantises each W2 row tile once.
 //
 // Method: DeepSeek V4.1 atlas "Mixture of experts" (Routed expert step:
 // E = W2 h); metrale moe_v41 module docs (Q3_K down projection on q8_1(h)).
@@ -29,10 +32,12 @@ namespace {
 
 constexpr int TM = PF_TM;          // weight rows per tile
 constexpr int TNQ = PF_TNQ;        // pairs per tile
-constexpr uint32_t B_STAGE = 2 * TNQ * 128;  // B tile: 64 hi rows + 64 lo rows of 64 fp16 (128-byte swizzle)
-constexpr int NSB = 8;             // B ring stages
-constexpr int NA = 8;              // A ring stages (32 tensor-memory columns each, from column 256)
-constexpr int NEW = 8;             // epilogue warps (0-7)
+constexpr int BBOX = 16;           // rows per B box: a tile loads only the rows of its pairs
+constexpr uint32_t B_STAGE = 2 * TNQ * 128;  // B tile: n hi rows, then n lo rows, of 64 fp16 (128-byte swizzle)
+constexpr uint32_t A_STAGE = TM * 128;       // A tile: 128 rows of 64 fp16 (128-byte swizzle)
+constexpr int NSB = 3;             // B ring stages
+constexpr int NA = 4;              // A ring stages
+constexpr int NEW = 8;             // epilogue warps (0-7): pairs 0-63 (warps 0-3) and 64-127 (warps 4-7)
 constexpr int NDW = 8;             // dequantising warps (8-15)
 constexpr int W_TMA = NEW + NDW;   // TMA issuer
 constexpr int W_MMA = W_TMA + 1;   // MMA issuer
@@ -44,7 +49,7 @@ constexpr uint32_t STG_WARP = 2u * 32 * Q3_PITCH * 4;
 constexpr uint32_t STG_BYTES = NDW * STG_WARP;
 
 struct KqArgs {
-  CUtensorMap map_bh, map_bl;           // B hi / lo parts: rows = pair positions, box {64 values, 64 rows}
+  CUtensorMap map_bh, map_bl;           // B hi / lo parts: rows = pair positions, box {64 values, 16 rows}
   const int4* tiles;                    // two int4 per tile: (expert, row tile, first pair, pairs), row pointer
   const int* n_tiles;
   int K;                                // contraction length I (a multiple of 256)
@@ -64,7 +69,7 @@ struct KqCtl {
   uint32_t abort;
 };
 
-constexpr uint32_t SMEM_BYTES = 1024 + NSB * B_STAGE + STG_BYTES + ((sizeof(KqCtl) + 15) & ~15u);
+constexpr uint32_t SMEM_BYTES = 1024 + NSB * B_STAGE + NA * A_STAGE + STG_BYTES + ((sizeof(KqCtl) + 15) & ~15u);
 static_assert(SMEM_BYTES <= 232448, "stages exceed the shared memory of a block");
 
 __device__ __forceinline__ uint64_t* bp(unsigned long long& b) { return reinterpret_cast<uint64_t*>(&b); }
@@ -77,13 +82,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// 8 f32 columns of the warp's TMEM lanes, without the wait (tcgen05.wait::ld
-// follows once for several loads)
-__device__ __forceinline__ void tmem_ld8_nw(uint32_t taddr, uint32_t* r) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Bounded wait of one thread; on a timeout the block's abort flag is set and
@@ -137,6 +135,7 @@ __device__ void run_mma(const KqArgs& g, KqCtl& C, uint32_t tmem, uint32_t smem_
                         uint64_t deadline) {
   const int nsb = g.K / QK;
   const uint64_t bdesc0 = umma_desc(smem_base);  // stage st adds st * B_STAGE / 16 to the address field
+  const uint64_t adesc0 = umma_desc(smem_base + NSB * B_STAGE);
   uint32_t gb = 0, ga = 0, gacc[2] = {0, 0};
   // a wait that is already satisfied costs one try; the bounded loop only runs when it is not
   auto wait = [&](unsigned long long& b, uint32_t par) -> bool {
@@ -144,12 +143,12 @@ __device__ void run_mma(const KqArgs& g, KqCtl& C, uint32_t tmem, uint32_t smem_
   };
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const Tile T = tile_of(g, t);
-    const uint32_t idesc = umma_idesc(TNQ + T.tnp, false);
+    const uint32_t idesc = umma_idesc(2 * T.tnp, false);
     for (int s = 0; s < nsb; ++s) {
       const int acc = s & 1;
       if (gacc[acc] > 0 && !wait(C.acc_empty[acc], (gacc[acc] - 1) & 1u)) goto out;
       tc_fence_after();
-      const uint32_t d = tmem + (uint32_t)(128 * acc);
+      const uint32_t d = tmem + (uint32_t)(256 * acc);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         const uint32_t bu = gb + (uint32_t)c, st = bu % NSB;
@@ -158,11 +157,11 @@ __device__ void run_mma(const KqArgs& g, KqCtl& C, uint32_t tmem, uint32_t smem_
         if (!wait(C.a_full[as], (au / NA) & 1u)) goto out;
         tc_fence_after();
         const uint64_t bd = bdesc0 + (uint64_t)(st * (B_STAGE >> 4));
-        const uint32_t ta = tmem + 256u + as * 32u;
-        umma_f16_ta(d, ta, bd, idesc, c ? 1u : 0u);
-        umma_f16_ta(d, ta + 8u, bd + 2u, idesc, 1u);
-        umma_f16_ta(d, ta + 16u, bd + 4u, idesc, 1u);
-        umma_f16_ta(d, ta + 24u, bd + 6u, idesc, 1u);
+        const uint64_t ad = adesc0 + (uint64_t)(as * (A_STAGE >> 4));
+        umma_f16(d, ad, bd, idesc, c ? 1u : 0u);
+        umma_f16(d, ad + 2u, bd + 2u, idesc, 1u);
+        umma_f16(d, ad + 4u, bd + 4u, idesc, 1u);
+        umma_f16(d, ad + 6u, bd + 6u, idesc, 1u);
         umma_commit(bp(C.a_empty[as]));
         umma_commit(bp(C.b_empty[st]));
       }
@@ -186,9 +185,11 @@ __device__ void run_tma(const KqArgs& g, KqCtl& C, uint32_t smem_base, int ntile
         const uint32_t bu = gb++, st = bu % NSB;
         if (bu >= NSB && !kwait(C, C.b_empty[st], (bu / NSB - 1) & 1u, deadline, g.status)) goto out;
         const uint32_t dst = smem_base + st * B_STAGE;
-        mbar_arrive_expect_tx(bp(C.b_full[st]), B_STAGE);
-        tma_load_2d(dst, &g.map_bh, QK * s + 64 * c, T.col0, bp(C.b_full[st]));
-        tma_load_2d(dst + TNQ * 128u, &g.map_bl, QK * s + 64 * c, T.col0, bp(C.b_full[st]));
+        mbar_arrive_expect_tx(bp(C.b_full[st]), 2u * (uint32_t)T.tnp * 128u);
+        for (int r = 0; r < T.tnp; r += BBOX) {
+          tma_load_2d(dst + (uint32_t)r * 128u, &g.map_bh, QK * s + 64 * c, T.col0 + r, bp(C.b_full[st]));
+          tma_load_2d(dst + (uint32_t)(T.tnp + r) * 128u, &g.map_bl, QK * s + 64 * c, T.col0 + r, bp(C.b_full[st]));
+        }
       }
     }
   }
@@ -203,6 +204,9 @@ out:
 }
 
 // --------------------------------------------------------- dequantisers
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -222,13 +226,13 @@ struct UnitCursor {
 // = one super-block: the 4-byte aligned 28-word window around the row's
 // 110-byte Q3_K block (2-byte aligned), realigned with one byte permute per
 // word.  A value is (code - 32) * q with q = lo + 4 hb - 4 (exact in fp16).
-__device__ void run_dequant_q3k(const KqArgs& g, KqCtl& C, uint32_t tmem, uint32_t* stg, int ntiles,
+__device__ void run_dequant_q3k(const KqArgs& g, KqCtl& C, uint32_t a_smem, uint32_t* stg, int ntiles,
                                 uint64_t deadline) {
   const int w = (threadIdx.x >> 5) - NEW;  // 0..7
   const int lane = threadIdx.x & 31;
   const int hf = w >> 2, quarter = w & 3;
+  const int row = quarter * 32 + lane;  // this thread's row of the tile
   const int nsb = g.K / QK;
-  const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16) + 256u;
   const uint32_t stg_s = smem_u32(stg);
   const __half2 m1028 = u2h(0xE404E404u);  // -1028 in both halves
   uint32_t ga = 0;  // chunk c of the n-th super-block walked is use 4 n + c of the ring
@@ -307,8 +311,8 @@ __device__ void run_dequant_q3k(const KqArgs& g, KqCtl& C, uint32_t tmem, uint32
 #pragma unroll
     for (int cc = 0; cc < 2 && ok; ++cc) {
       const int c = 2 * hf + cc;
-      const uint32_t au = ga + (uint32_t)c, as = au % 8;
-      if (au >= 8 && !kwait_warp(C, C.a_empty[as], (au / 8 - 1) & 1u, deadline, g.status)) {
+      const uint32_t au = ga + (uint32_t)c, as = au % NA;
+      if (au >= NA && !kwait_warp(C, C.a_empty[as], (au / NA - 1) & 1u, deadline, g.status)) {
         ok = false;
         break;
       }
@@ -336,11 +340,15 @@ __device__ void run_dequant_q3k(const KqArgs& g, KqCtl& C, uint32_t tmem, uint32
             o[2 * wd] = h2u(__hmul2(__hadd2(u2h(prmt(q, 0x64646464u, 0x4140u)), m1028), ds));
             o[2 * wd + 1] = h2u(__hmul2(__hadd2(u2h(prmt(q, 0x64646464u, 0x4342u)), m1028), ds));
           }
-          tmem_st8(lane_addr + (uint32_t)(as * 32 + 16 * jb + 8 * l16), o);
+          // the 16 values are K 32 jb + 16 l16 .. + 15 of the chunk: two 16-byte pieces
+          const uint32_t base = a_smem + as * A_STAGE;
+          sts128(base + swz(row, 4 * jb + 2 * l16), o[0], o[1], o[2], o[3]);
+          sts128(base + swz(row, 4 * jb + 2 * l16 + 1), o[4], o[5], o[6], o[7]);
         }
       }
-      tmem_wait_st();
-      warp_arrive(C.a_full[as]);
+      fence_async_smem();  // the tensor cores read A through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bp(C.a_full[as]));
     }
     if (!ok) break;
     ga += 4;
@@ -352,8 +360,6 @@ __device__ void run_dequant_q3k(const KqArgs& g, KqCtl& C, uint32_t tmem, uint32
 }
 
 // ------------------------------------------------------------- epilogue
-// Drain of one accumulator: R[p] += c * (hi[p] + lo[p]) for the tile's pairs
-// (hi at columns 0.., lo at columns 64..).
 __device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -362,13 +368,16 @@ __device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void drain(uint32_t acc_lane, int tnp, float c, float (&R)[TNQ]) {
+// Drain of one accumulator for np of the warp group's pairs (np a multiple of
+// 16, at most 64): R[p] += c * (hi[p] + lo[p]), hi at column hi0 + p and lo
+// at column lo0 + p of the warp's lanes.
+__device__ __forceinline__ void drain(uint32_t hi0, uint32_t lo0, int np, float c, float (&R)[64]) {
 #pragma unroll
-  for (int q = 0; q < TNQ / 16; ++q) {
-    if (16 * q < tnp) {  // warp-uniform
+  for (int q = 0; q < 4; ++q) {
+    if (16 * q < np) {  // warp-uniform
       uint32_t hi[16], lo[16];
-      tmem_ld16_nw(acc_lane + (uint32_t)(16 * q), hi);
-      tmem_ld16_nw(acc_lane + (uint32_t)(TNQ + 16 * q), lo);
+      tmem_ld16_nw(hi0 + (uint32_t)(16 * q), hi);
+      tmem_ld16_nw(lo0 + (uint32_t)(16 * q), lo);
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 16; ++j) R[16 * q + j] = fmaf(c, __uint_as_float(hi[j]) + __uint_as_float(lo[j]), R[16 * q + j]);
@@ -376,81 +385,45 @@ __device__ __forceinline__ void drain(uint32_t acc_lane, int tnp, float c, float
   }
 }
 
-// The running sums of one warp group go to the other group through tensor
-// memory: into columns 0..63 of accumulator `acc` of the same lanes (the two
-// groups cover the same lane quarters), which the writing group has drained
-// and not yet handed back to the MMA issuer.
-__device__ __forceinline__ void stash_sums(uint32_t acc_lane, int tnp, const float (&R)[TNQ]) {
-#pragma unroll
-  for (int q = 0; q < TNQ / 8; ++q) {
-    if (8 * q < tnp) {
-      uint32_t v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __float_as_uint(R[8 * q + j]);
-      tmem_st8(acc_lane + (uint32_t)(8 * q), v);
-    }
-  }
-  tmem_wait_st();
-}
-
-// Down: warps 0-3 drain the even super-blocks' accumulator, 4-7 the odd
-// ones', each into running sums of its row; at the end of a tile the odd
-// sums go through tensor memory and the even warps write E = even + odd.
+// Warps 0-3 keep the running sums of pairs 0-63 of the tile, warps 4-7 those
+// of pairs 64-127, each for its quarter of the rows; both groups drain every
+// super-block's accumulator (the hi parts at columns 0..n-1, the lo parts at
+// n..2n-1) and then write their pairs of E.
 __device__ void run_epilogue_dn(const KqArgs& g, KqCtl& C, uint32_t tmem, int ntiles, uint64_t deadline) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int par = w >> 2, quarter = w & 3, r = quarter * 32 + lane;
+  const int grp = w >> 2, quarter = w & 3, r = quarter * 32 + lane;
   const int nsb = g.K / QK;
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-  const uint32_t acc_lane = lane_base + (uint32_t)(128 * par);
-  const int last_odd = (nsb & 1) ? nsb - 2 : nsb - 1;  // the odd group's last super-block (nsb > 1)
-  uint32_t gacc = 0;
+  uint32_t gacc[2] = {0, 0};
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const Tile T = tile_of(g, t);
     const int row = T.mt * TM + r;
     const uint8_t* rowp = T.rows + (size_t)r * g.a_row_bytes;
-    float R[TNQ];
+    const int p0 = 64 * grp;
+    const int np = min(64, T.tnp - p0);  // this group's columns (<= 0: none)
+    float R[64];
 #pragma unroll
-    for (int p = 0; p < TNQ; ++p) R[p] = 0.f;
+    for (int p = 0; p < 64; ++p) R[p] = 0.f;
     bool ok = true;
-    for (int s = par; s < nsb; s += 2) {
+    for (int s = 0; s < nsb; ++s) {
+      const int acc = s & 1;
       const uint8_t* dp = rowp + (size_t)s * Q3K_B + 108;
       const float c = half_bits_to_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(dp)));
-      if (ok && kwait_warp(C, C.acc_full[par], gacc & 1u, deadline, g.status)) {
+      if (ok && kwait_warp(C, C.acc_full[acc], gacc[acc] & 1u, deadline, g.status)) {
         tc_fence_after();
-        drain(acc_lane, T.tnp, c, R);
-        if (par == 0 || s != last_odd) warp_arrive(C.acc_empty[par]);
+        const uint32_t a = lane_base + (uint32_t)(256 * acc);
+        drain(a + (uint32_t)p0, a + (uint32_t)(T.tnp + p0), np, c, R);
+        warp_arrive(C.acc_empty[acc]);
       } else {
         ok = false;
       }
-      ++gacc;
+      ++gacc[acc];
     }
-    const bool two = nsb > 1;
-    if (par == 1 && two && ok) {
-      stash_sums(acc_lane, T.tnp, R);
-      tc_fence_before();
-    }
-    named_bar_sync(1, NEW * 32);
-    if (par == 0 && ok) {
-      tc_fence_after();
+    if (ok) {
 #pragma unroll
-      for (int q = 0; q < TNQ / 8; ++q) {
-        if (8 * q < T.tnp) {
-          uint32_t u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          if (two) {
-            tmem_ld8_nw(lane_base + 128u + (uint32_t)(8 * q), u);
-            tmem_wait_ld();
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int p = 8 * q + j;
-            if (p < T.ncol) g.out_e[(size_t)(T.col0 + p) * g.out_ld + row] = R[p] + __uint_as_float(u[j]);
-          }
-        }
-      }
-      tc_fence_before();
+      for (int p = 0; p < 64; ++p)
+        if (p < np && p0 + p < T.ncol) g.out_e[(size_t)(T.col0 + p0 + p) * g.out_ld + row] = R[p];
     }
-    named_bar_sync(1, NEW * 32);
-    if (par == 1 && two && ok) warp_arrive(C.acc_empty[1]);
   }
 }
 
@@ -458,8 +431,8 @@ __device__ void run_epilogue_dn(const KqArgs& g, KqCtl& C, uint32_t tmem, int nt
 __global__ void __launch_bounds__(NTHR, 1) k_down_gemm(const __grid_constant__ KqArgs g) {
   extern __shared__ __align__(1024) uint8_t raw_smem[];
   uint8_t* sm = raw_smem + ((1024u - (smem_u32(raw_smem) & 1023u)) & 1023u);
-  uint32_t* stg = reinterpret_cast<uint32_t*>(sm + NSB * B_STAGE);
-  KqCtl& C = *reinterpret_cast<KqCtl*>(sm + NSB * B_STAGE + STG_BYTES);
+  uint32_t* stg = reinterpret_cast<uint32_t*>(sm + NSB * B_STAGE + NA * A_STAGE);
+  KqCtl& C = *reinterpret_cast<KqCtl*>(sm + NSB * B_STAGE + NA * A_STAGE + STG_BYTES);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntiles = __ldg(g.n_tiles);
   if ((int)blockIdx.x >= ntiles) return;
@@ -475,7 +448,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_down_gemm(const __grid_constant__ K
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bp(C.acc_full[i]), 1);
-      mbar_init(bp(C.acc_empty[i]), 4);  // one arrival per epilogue warp of the accumulator
+      mbar_init(bp(C.acc_empty[i]), NEW);  // one arrival per epilogue warp
     }
     mbar_init(bp(C.done), 1);
     C.abort = 0u;
@@ -491,7 +464,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_down_gemm(const __grid_constant__ K
   if (warp < NEW) {
     run_epilogue_dn(g, C, tmem, ntiles, deadline);
   } else if (warp < NEW + NDW) {
-    run_dequant_q3k(g, C, tmem, stg + (size_t)(warp - NEW) * (STG_WARP / 4), ntiles, deadline);
+    run_dequant_q3k(g, C, smem_base + NSB * B_STAGE, stg + (size_t)(warp - NEW) * (STG_WARP / 4), ntiles, deadline);
   } else if (warp == W_TMA) {
     if (lane == 0) run_tma(g, C, smem_base, ntiles, deadline);
   } else {
@@ -514,8 +487,8 @@ __global__ void __launch_bounds__(NTHR, 1) k_down_gemm(const __grid_constant__ K
 // ---------------------------------------------------------------- host
 int launch_kq_gemm(const KqLaunch& L, cudaStream_t s) {
   KqArgs g{};
-  if (!make_map_b16(&g.map_bh, L.bh, (uint64_t)L.K, (uint64_t)L.b_rows, TNQ) ||
-      !make_map_b16(&g.map_bl, L.bl, (uint64_t)L.K, (uint64_t)L.b_rows, TNQ))
+  if (!make_map_b16(&g.map_bh, L.bh, (uint64_t)L.K, (uint64_t)L.b_rows, BBOX) ||
+      !make_map_b16(&g.map_bl, L.bl, (uint64_t)L.K, (uint64_t)L.b_rows, BBOX))
     return MOE_ERR_CUDA;
   g.tiles = L.tiles; g.n_tiles = L.n_tiles; g.K = L.K; g.a_row_bytes = L.a_row_bytes; g.out_ld = L.out_ld;
   g.out_e = L.out_e; g.status = L.status; g.timeout_ns = L.timeout_ns;

@@ -93,17 +93,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x
       : "memory");
 }
 
-// TMA gather of four rows y0..y3 (box {64 elements, 1 row}) at column x into
-// four consecutive 128-byte shared-memory rows, completing on `bar`.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int x, int y0, int y1, int y2, int y3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // 8 consecutive 32-bit columns of this thread's TMEM lane (the warp's 32
 // lanes start at taddr's lane field).
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* w) {

@@ -31,7 +31,7 @@ MAX_ABS_REL = 1e-2
 # different h elements are nearly orthogonal).
 OUT_MAX_ABS_REL = 2e-3
 FLIP_KAPPA = 2.0 ** -18
-FLIP_LOOK = 0.25
+FLIP_LOOK = 0.5
 FLIP_MIN = 0.1
 FLIP_TAKE = (0.75, 1.5)
 FLIP_MAX = 2048
