@@ -623,11 +623,11 @@ def _mem_available() -> int:
 
 
 def streamed_in_child(args):
-    """The streamed leg in a process of its own.  In the process that ran the
-    other legs its timings depended on them (same box, same code): after the
-    e2e leg the prefetch runs took 1.2-1.3 ms per layer call instead of 0.39,
-    after the prefill leg single runs took up to 1.0 ms instead of 0.47; alone,
-    or after the CPU baseline, three repetitions agreed within 2%."""
+    """The streamed leg in a process of its own, after the other legs have
+    released their device memory.  (Run after them in one process, single
+    runs took 0.7-1.3 ms per layer call instead of 0.39-0.47; run_streamed's
+    untimed pass over the arena is what removed that, this keeps the legs
+    apart as well.)"""
     import gc
 
     import torch
@@ -642,7 +642,7 @@ def streamed_in_child(args):
         return {"skipped": "streamed leg failed: " + (p.stderr.strip().splitlines() or ["?"])[-1]}
     lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
     sm = json.loads(lines[-1]) if lines else {"skipped": "streamed leg printed no result"}
-    sm["process"] = "a child process of its own (its timings depended on the legs run before it in one process)"
+    sm["process"] = "a child process of its own, after one untimed host -> HBM pass over the arena"
     return sm
 
 
@@ -683,6 +683,11 @@ def run_streamed(args, local_rank):
         for l in range(Ls):
             fill_experts_gpu(w, l, stagebuf)
             arena[l].copy_(stagebuf)
+        # one untimed host -> HBM pass over the whole arena before any timed
+        # run (the first timed run over freshly registered pages was slow)
+        for l in range(Ls):
+            stagebuf.copy_(arena[l], non_blocking=True)
+        torch.cuda.synchronize()
         # the link's own rate: plain arena -> HBM copies of whole expert slots
         nprobe = min(16, w.n_routed)
         probe = stagebuf[:nprobe]
