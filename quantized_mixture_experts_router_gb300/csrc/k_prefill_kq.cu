@@ -94,7 +94,7 @@ __device__ __forceinline__ bool kwait(KqCtl& C, unsigned long long& bar, uint32_
   return false;
 }
 
-// The same for a whole warp (lane 0 waits, the verdict is shared).
+// The same for a whole warp (lane 0 waits, the result is shared).
 __device__ __forceinline__ bool kwait_warp(KqCtl& C, unsigned long long& bar, uint32_t parity, uint64_t deadline,
                                            unsigned* status) {
   bool ok = true;

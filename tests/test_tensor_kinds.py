@@ -3,7 +3,7 @@
 The prefill design question "int8 tcgen05 MMA tiles or fp16 ones" is settled
 by the toolchain: ptxas refuses tcgen05.mma .kind::i8 for sm_103a (GB300) and
 accepts the same instruction for sm_100a, while .kind::f16 is accepted for
-sm_103a.  Only the compiler's verdict is read here; no output is inspected."""
+sm_103a.  Only the compiler's answer is read here; no output is inspected."""
 import os
 import subprocess
 
