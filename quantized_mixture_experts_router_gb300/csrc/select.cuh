@@ -336,42 +336,53 @@ static __device__ __noinline__ void route_token_warp_r12(const float* __restrict
     kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
   const float eps = 0x1.0p-18f * (smax + kmax) + 0x1.0p-126f;
-  uint32_t taken = 0;
   float prev_key = 0.f;
   bool resolved = true;
   int my_id = 0;  // lane r < k: pick r
   float my_s = 0.f;
   const int rounds = k < N ? k + 1 : k;
-  // order-preserving key bits (the high word of rank_key), computed once
+  // order-preserving key bits (the high word of rank_key), computed once; the
+  // scores go to the scratch by expert id, read back for the picks
   uint32_t ku[PL];
+  uint32_t live = 0;  // bit i: entry i exists and is not taken
 #pragma unroll
-  for (int i = 0; i < PL; ++i) ku[i] = (uint32_t)(rank_key(kf[i], 0) >> 32);
+  for (int i = 0; i < PL; ++i) {
+    ku[i] = (uint32_t)(rank_key(kf[i], 0) >> 32);
+    if (lane + 32 * i < N) {
+      live |= 1u << i;
+      scratch[lane + 32 * i] = sc[i];
+    }
+  }
+  __syncwarp();
 #pragma unroll 1
   for (int r = 0; r < rounds; ++r) {
-    // the lane's best untaken key (ties: the lower index, i.e. the lower id)
-    uint32_t best = 0;
-    int bi = -1;
-    float bk = 0.f, bs = 0.f;
+    // the lane's best untaken key, ties to the lower index (the lower id):
+    // a branch-free tree maximum of (key bits, 255 - index), 0 = no entry
+    unsigned long long v[PL];
 #pragma unroll
-    for (int i = 0; i < PL; ++i) {
-      if (lane + 32 * i < N && !(taken >> i & 1u) && (bi < 0 || ku[i] > best)) {
-        best = ku[i]; bi = i; bk = kf[i]; bs = sc[i];
-      }
-    }
+    for (int i = 0; i < PL; ++i)
+      v[i] = (live >> i & 1u) ? (((unsigned long long)ku[i] << 32) | (unsigned long long)(255 - i)) : 0ull;
+#pragma unroll
+    for (int w = 1; w < PL; w <<= 1)
+#pragma unroll
+      for (int i = 0; i + w < PL; i += 2 * w) v[i] = v[i] > v[i + w] ? v[i] : v[i + w];
+    const bool has = v[0] != 0ull;
+    const uint32_t best = (uint32_t)(v[0] >> 32);
+    const int bi = 255 - (int)(v[0] & 255ull);
     // the warp's largest key, then the lowest id among the lanes holding it
     // (a lane with nothing left offers no id; NaN keys, bits 0, still win
     // over nothing)
-    const uint32_t top = __reduce_max_sync(0xffffffffu, best);
-    const uint32_t cand = (bi >= 0 && best == top) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
+    const uint32_t top = __reduce_max_sync(0xffffffffu, has ? best : 0u);
+    const uint32_t cand = (has && best == top) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
     const int win = (int)__reduce_min_sync(0xffffffffu, cand);
-    const float wk = __shfl_sync(0xffffffffu, bk, win & 31);
-    const float ws = __shfl_sync(0xffffffffu, bs, win & 31);
-    if ((win & 31) == lane) taken |= 1u << (win >> 5);
+    // the winner's key from its bits (the inverse of rank_key's map)
+    const float wk = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
+    if ((win & 31) == lane) live &= ~(1u << (win >> 5));
     if (r > 0 && !(prev_key - wk > 2.0f * eps)) resolved = false;
     prev_key = wk;
     if (r < k && lane == r) {
       my_id = win;
-      my_s = ws;
+      my_s = scratch[win];
     }
   }
   if (!resolved) {
