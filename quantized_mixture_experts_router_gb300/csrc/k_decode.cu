@@ -244,10 +244,15 @@ __device__ __noinline__ float4 q2k_rows4_dot(uint32_t w, uint32_t rb, int U, uin
     load_unit<S>(xr, xs, xg, (uint32_t)u * UB);
     const uint8_t* blk = smem_base() + w + (u >> 2) * Q2K_B;
     const int c = u & 3;
-    a0 += q2k_unit_dot(blk, c, xr);
-    a1 += q2k_unit_dot(blk + rb, c, xr);
-    a2 += q2k_unit_dot(blk + 2 * rb, c, xr);
-    a3 += q2k_unit_dot(blk + 3 * rb, c, xr);
+    // one copy of the unit dot in the loop body (a smaller instruction footprint)
+#pragma unroll 1
+    for (int r = 0; r < 4; ++r) {
+      const float d = q2k_unit_dot(blk + r * rb, c, xr);
+      a0 += r == 0 ? d : 0.f;
+      a1 += r == 1 ? d : 0.f;
+      a2 += r == 2 ? d : 0.f;
+      a3 += r == 3 ? d : 0.f;
+    }
   }
 #pragma unroll
   for (int o = 8; o; o >>= 1) {
