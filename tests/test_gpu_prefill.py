@@ -294,3 +294,19 @@ def test_prefill_m4096_outliers_full_shape():
     # the outlier rows on their own (their errors would vanish in the whole)
     rows = W.outlier_rows(w, 0)
     assert_output(res["out"][rows], r, "outlier rows", rows=rows)
+
+
+@pytest.mark.slow
+def test_prefill_at_the_token_limit():
+    """max_tokens = 65536, the configuration's limit: 458,752 pair rows, so the
+    per-pair buffers hold more than 2^31 values (every index into them is
+    64-bit).  Properties of every token, and the oracle on sampled tokens:
+    the first and last, outlier rows and a seeded spread."""
+    w = W.WORKLOADS["prefill_m4096_outliers"].with_(m=65536)
+    dl = stage_layer(w, 0, experts_on_gpu=True)
+    res = gpu_forward(dl)
+    _full_properties(w, 0, res)
+    rng = np.random.default_rng(11)
+    out_rows = W.outlier_rows(w, 0)
+    tokens = np.unique(np.concatenate([[0, w.m - 1], out_rows[:4], rng.choice(w.m, 10, replace=False)]))
+    _check(w, 0, res, tokens=tokens)
