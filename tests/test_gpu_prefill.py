@@ -310,3 +310,17 @@ def test_prefill_at_the_token_limit():
     out_rows = W.outlier_rows(w, 0)
     tokens = np.unique(np.concatenate([[0, w.m - 1], out_rows[:4], rng.choice(w.m, 10, replace=False)]))
     _check(w, 0, res, tokens=tokens)
+
+
+@pytest.mark.parametrize("path,m", [("decode", 4), ("prefill", 40)])
+@pytest.mark.parametrize("n", [1, 16])
+def test_every_expert_picked(path, m, n):
+    """The degenerate routings: one expert in all (k = N = 1, no
+    renormalisation at k = 1) and every expert picked (k = N = 16, no
+    (k+1)-th key to separate), on both paths."""
+    w = W.WORKLOADS["tiny"].with_(m=m, n_routed=n, topk=n)
+    dl = stage_layer(w, 0, experts_on_gpu=False)
+    res = gpu_forward(dl, path=Q.MOE_PATH_DECODE if path == "decode" else Q.MOE_PATH_PREFILL)
+    assert res["status"] == 0
+    assert np.array_equal(np.sort(res["topk_idx"], axis=1), np.tile(np.arange(n), (m, 1)))
+    _check(w, 0, res)
