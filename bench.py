@@ -64,7 +64,7 @@ def parse():
     ap.add_argument("--streamed-slots", type=int, default=256, help="HBM expert slots of the streamed leg")
     ap.add_argument("--streamed-tokens", type=int, default=64, help="timed tokens of the streamed leg")
     ap.add_argument("--prefetch-k", type=int, default=6, help="predicted next-layer experts fetched ahead")
-    ap.add_argument("--streamed-reps", type=int, default=2, help="repetitions of each streamed configuration")
+    ap.add_argument("--streamed-reps", type=int, default=3, help="repetitions of each streamed configuration")
     ap.add_argument("--streamed-only", action="store_true",
                     help="run only the streamed leg and print its JSON object (the main run starts it this way)")
     ap.add_argument("--mma-rates", action="store_true",
@@ -711,7 +711,8 @@ def run_streamed(args, local_rank):
         stream = torch.cuda.current_stream()
         copy_stream = torch.cuda.Stream(device=dev)
         runs = []
-        # each configuration twice, alternating: repetitions on one box have differed by up to 2.7x
+        # each configuration several times, alternating: single runs on one box have taken up to 2.8x the
+        # usual time (copies at ~48 GB/s instead of ~160), in either configuration, cause not established
         plan_runs = [(rep, P) for rep in range(args.streamed_reps)
                      for P in ([0, args.prefetch_k] if args.prefetch_k > 0 else [0])]
         for rep, P in plan_runs:
@@ -756,7 +757,10 @@ def run_streamed(args, local_rank):
                          "frac_of_link": dd["bytes_copied"] / sec / 1e9 / link_gbs})
             cache.close()
             del slots, tables, cache
+        medians = {str(P): statistics.median(r["ms_per_layer_call"] for r in runs if r["prefetch_k"] == P)
+                   for P in sorted(set(r["prefetch_k"] for r in runs))}
         return {"workload": w.name + " (experts streamed)", "arena_layers": Ls, "arena_bytes": arena.numel(),
+                "median_ms_per_layer_call": medians,
                 "slots": S, "slot_bytes": slot, "hbm_slot_bytes": S * slot, "timed_tokens": args.streamed_tokens,
                 "layers_per_token": Ls, "link_gbs": link_gbs,
                 "link": "arena -> HBM rate of plain copies of whole expert slots, measured in this run",
