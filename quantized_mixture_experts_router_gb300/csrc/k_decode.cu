@@ -804,6 +804,8 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
         bulk_g2s(smem_base() + p.sm_bias, p.bias, (uint32_t)(p.N * 4), bar(C.cbar[CB_BIAS]));
       }
     }
+    // every weight byte is read once per call: its lines go first when L2 needs room
+    const uint64_t evict_first = l2_evict_first_policy();
     uint32_t n = 0;  // stages issued
     uint32_t j = 0;  // items started
     bool ok = true;
@@ -998,8 +1000,8 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
         C.hdr[slot] = h;
         uint8_t* dst = smem_base() + (size_t)slot * SB;
         mbar_arrive_expect_tx(bar(C.full[slot]), a ? (b ? 2u * bytes : bytes) : 0u);
-        if (a) bulk_g2s(dst, a, bytes, bar(C.full[slot]));
-        if (a && b) bulk_g2s(dst + boff, b, bytes, bar(C.full[slot]));
+        if (a) bulk_g2s_hint(dst, a, bytes, bar(C.full[slot]), evict_first);
+        if (a && b) bulk_g2s_hint(dst + boff, b, bytes, bar(C.full[slot]), evict_first);
       }
       ok = __all_sync(0xffffffffu, lane_ok);
       n += (uint32_t)ns;
