@@ -644,6 +644,24 @@ __device__ __noinline__ void task_dn_b(const DecodeParams& p, Ctl& C, uint32_t s
   }
 }
 
+// An L2 policy that makes the lines a load brings in the first to be evicted:
+// for data read once per call (expert weights), so that the call's small,
+// reused data (instructions, activations, counters) keeps its place in L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// bulk_g2s with an L2 cache policy (l2_evict_first_policy)
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 // ------------------------------------------------------- item completion
 __device__ __noinline__ void complete_item(const DecodeParams& p, Ctl& C, Item it, float* ib, uint64_t deadline) {
   const int lane = threadIdx.x & 31;
