@@ -914,7 +914,8 @@ def main():
              "roofline": roofline(pw, pf["distinct"], pf["per_call_ms"],
                                   ("k_decode_layer (the whole layer call, one launch)" if pf["launches_per_call"] == 1
                                    else f"the prefill kernels of one layer call ({pf['launches_per_call']} launches)"),
-                                  recorded_traffic(pw.name)),
+                                  # the recorded traffic is for the workload's own token count
+                                  recorded_traffic(pw.name) if pw.m == W.WORKLOADS[pw.name].m else None),
              "gpu_launches": pf["launches_per_call"] * pf["K"], "clocks": pf["clocks"],
              "dtype": ("int8-dp4a, f32 accumulate" if decode_like else
                        "fp16 tensor-core GEMMs on exact-integer K-quant weights, bf16 router/shared, f32 accumulate")}
