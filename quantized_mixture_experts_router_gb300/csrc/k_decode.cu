@@ -8,9 +8,10 @@
 // items while it does not (and when the routed gate/up items run out), and
 // the routed down items last, and streams each item's raw weight rows into the ring as stages with 1-D
 // bulk copies (cp.async.bulk, completing on the stage's mbarrier).  Each stage
-// is one TASK, taken and finished by a single consumer warp; the warps of the
-// block share an item through a small shared-memory state (a task counter and
-// a result buffer), and the warp finishing an item's last task completes it:
+// is one TASK, taken and finished by a pair of consumer warps (each does half
+// of the stage's rows); the pairs of the block share an item through a small
+// shared-memory state (a task counter and a result buffer), and the pair
+// finishing an item's last task completes it:
 //   router item   -> counts it; the planner warp of every block then selects
 //                    the experts and groups the pairs into its own plan
 //   gate/up item  -> SwiGLU is done per task; the 32-row group of h goes to
@@ -46,7 +47,8 @@ namespace moe {
 
 namespace {
 
-constexpr int NCW = 8;               // consumer warps
+constexpr int NCW = 16;              // consumer warps
+constexpr int NPAIR = NCW / 2;       // consumer pairs: a stage is one task of a pair of warps
 constexpr int W_PROD = NCW;          // the producer warp
 constexpr int W_PLAN = NCW + 1;      // the planner warp: this block's copy of the routing
 constexpr int NTH = (NCW + 2) * 32;
@@ -63,7 +65,7 @@ constexpr int SDR = 2;               // shared bf16 down rows per stage
 constexpr int UB = UNIT_WORDS * 4;   // bytes of one activation unit
 // the producer ends the ring with one stop stage per consumer; a stop stage
 // is never released, so all of them must fit in the ring at once
-static_assert(NCW <= NST, "more consumer warps than ring stages");
+static_assert(NPAIR <= NST, "more consumer pairs than ring stages");
 static_assert(GR == 4 && RR == 1 && SDR == 2, "the row routines are instantiated for these row counts");
 static_assert(SB % 16 == 0, "stages start on 16-byte boundaries");
 
@@ -97,6 +99,8 @@ struct Ctl {
   unsigned rdy;                   // RQ_* bits: inputs ready for every warp of the block
   unsigned xq;                    // consumer warps done with their share of q8_1(x)
   unsigned sink;                  // status bits of the planner's warm-up pass (discarded)
+  unsigned pair_n[NPAIR];         // the stage each pair works on (written by its leader)
+  unsigned pair_ok[NPAIR];        // 0: the leader's wait for the stage failed
 };
 
 __device__ __forceinline__ uint8_t* smem_base() {
@@ -235,7 +239,7 @@ __device__ __noinline__ float4 bf16_rows_dot(uint32_t w, uint32_t rs, uint32_t v
 // in the unit layout, by a half-warp (16 lanes, 1/16 of the units each).
 // Every lane of the half returns the four sums.
 template <bool S>
-__device__ __noinline__ float4 q2k_rows4_dot(uint32_t w, uint32_t rb, int U, uint32_t xs, const uint8_t* xg) {
+__device__ __noinline__ float4 q2k_rows4_dot(uint32_t w, uint32_t rb, int nr, int U, uint32_t xs, const uint8_t* xg) {
   const int l = threadIdx.x & 15;
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 1
@@ -246,7 +250,7 @@ __device__ __noinline__ float4 q2k_rows4_dot(uint32_t w, uint32_t rb, int U, uin
     const int c = u & 3;
     // one copy of the unit dot in the loop body (a smaller instruction footprint)
 #pragma unroll 1
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < nr; ++r) {
       const float d = q2k_unit_dot(blk + r * rb, c, xr);
       a0 += r == 0 ? d : 0.f;
       a1 += r == 1 ? d : 0.f;
@@ -268,14 +272,15 @@ __device__ __noinline__ float4 q2k_rows4_dot(uint32_t w, uint32_t rb, int U, uin
 // lanes of a row group (1/4 of the units each); the four lanes return the sum.
 template <bool S>
 __device__ __noinline__ float q3k_row_dot(uint32_t rowp, int U2, uint32_t hs, const uint8_t* hg) {
-  const int q = threadIdx.x & 3;
+  const int q = threadIdx.x & 7;
   float acc = 0.f;
 #pragma unroll 1
-  for (int u = q; u < U2; u += 4) {
+  for (int u = q; u < U2; u += 8) {
     XUnit hr;
     load_unit<S>(hr, hs, hg, (uint32_t)u * UB);
     acc += q3k_unit_dot(smem_base() + rowp + (u >> 2) * Q3K_B, u & 3, hr);
   }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   return acc;
@@ -496,10 +501,12 @@ __device__ __noinline__ void quantize_x_smem(const DecodeParams& p, int first, i
   }
 }
 
-// Block-local work, NCW tasks per block issued after the block's router rows:
-// share `part` of q8_1(x) into shared memory.  Eight warps run the code at
-// once, so its instruction-cache misses are paid once per SM, not per warp.
+// Block-local work, one task per consumer pair issued after the block's
+// router rows: each warp quantises share `part` (of NCW) of q8_1(x) into
+// shared memory.  All consumer warps run the code at once, so its
+// instruction-cache misses are paid once per SM, not per warp.
 __device__ __noinline__ void task_local(const DecodeParams& p, Ctl& C, int part, uint64_t deadline) {
+  // part: this warp's share, 0 .. NCW - 1
   const int lane = threadIdx.x & 31;
   if (p.sm_x) {
     require(p, C, RQ_XB, deadline);
@@ -554,7 +561,7 @@ __device__ __noinline__ void task_shgu_b(const DecodeParams& p, Ctl& C, uint32_t
 // q8_1(x) units of the item's tokens: half-warp 0 takes W1, half-warp 1 W3.
 // h of the rows -> item buffer.
 __device__ __noinline__ void task_gu_q(const DecodeParams& p, Ctl& C, uint32_t st, int slot, int stg, float* ib,
-                                       uint64_t deadline) {
+                                       int part, uint64_t deadline) {
   const int lane = threadIdx.x & 31, half = lane >> 4;
   const uint32_t rb = (p.D / QK) * Q2K_B;
   const int U = p.D / 64;
@@ -568,23 +575,20 @@ __device__ __noinline__ void task_gu_q(const DecodeParams& p, Ctl& C, uint32_t s
     if (plan->exp_ptr[slot][0] == 0ull) return;
   }
   require(p, C, RQ_XU, deadline);
-  const uint32_t w = st + (uint32_t)half * GR * rb;
+  const uint32_t w = st + (uint32_t)half * GR * rb + (uint32_t)(2 * part) * rb;
   const uint32_t xstride = unit_bytes(p.D);
 #pragma unroll 1
   for (int tt = 0; tt < ntok; ++tt) {
     const int tok = shared ? tt : plan->pair_tok[pair0 + tt];
-    const float4 a = p.sm_x ? q2k_rows4_dot<true>(w, rb, U, p.sm_x + (uint32_t)tok * xstride, nullptr)
-                            : q2k_rows4_dot<false>(w, rb, U, 0u,
+    const float4 a = p.sm_x ? q2k_rows4_dot<true>(w, rb, 2, U, p.sm_x + (uint32_t)tok * xstride, nullptr)
+                            : q2k_rows4_dot<false>(w, rb, 2, U, 0u,
                                                    reinterpret_cast<const uint8_t*>(p.xu) + (size_t)tok * xstride);
     // lanes 0..15 hold the W1 sums, lanes 16..31 the W3 sums
     const float u0 = __shfl_sync(0xffffffffu, a.x, 16), u1 = __shfl_sync(0xffffffffu, a.y, 16);
-    const float u2 = __shfl_sync(0xffffffffu, a.z, 16), u3 = __shfl_sync(0xffffffffu, a.w, 16);
     if (lane == 0) {
-      float* o = ib + (size_t)stg * GR * p.m + tt;
+      float* o = ib + ((size_t)stg * GR + 2 * part) * p.m + tt;
       o[0] = swiglu_f32(a.x, u0, p.swiglu_limit);
       o[p.m] = swiglu_f32(a.y, u1, p.swiglu_limit);
-      o[2 * p.m] = swiglu_f32(a.z, u2, p.swiglu_limit);
-      o[3 * p.m] = swiglu_f32(a.w, u3, p.swiglu_limit);
     }
   }
 }
@@ -594,8 +598,8 @@ __device__ __noinline__ void task_gu_q(const DecodeParams& p, Ctl& C, uint32_t s
 // item buffer row pair*DG (unweighted); shared (slot < 0): the shared
 // expert's rows -> item buffer row t*DG.
 __device__ __noinline__ void task_dn_q(const DecodeParams& p, Ctl& C, uint32_t st, int slot, float* ib,
-                                       uint64_t deadline) {
-  const int lane = threadIdx.x & 31, row = lane >> 2, q = lane & 3;
+                                       int part, uint64_t deadline) {
+  const int lane = threadIdx.x & 31, row = 4 * part + (lane >> 3), q = lane & 7;
   const uint32_t rb2 = (p.I / QK) * Q3K_B;
   const int U2 = p.I / 64;
   const uint32_t hstride = unit_bytes(p.I);
@@ -630,17 +634,15 @@ __device__ __noinline__ void task_dn_q(const DecodeParams& p, Ctl& C, uint32_t s
 
 // SDR rows of the bf16 shared down matrix against h (bf16 [m, I]) -> item buffer
 __device__ __noinline__ void task_dn_b(const DecodeParams& p, Ctl& C, uint32_t st, int part, float* ib,
-                                       uint64_t deadline) {
+                                       int half, uint64_t deadline) {
   const int lane = threadIdx.x & 31;
   require(p, C, RQ_HS, deadline);
 #pragma unroll 1
   for (int t = 0; t < p.m; ++t) {
-    const float4 s = p.sm_hs ? bf16_rows_dot<2, true>(st, 2u * p.I, p.sm_hs + 2u * t * p.I, nullptr, p.I / 8)
-                             : bf16_rows_dot<2, false>(st, 2u * p.I, 0u, p.shh + (size_t)t * 2 * p.I, p.I / 8);
-    if (lane == 0) {
-      float* o = ib + (size_t)t * DG + part * SDR;
-      o[0] = s.x; o[1] = s.y;
-    }
+    const uint32_t row = st + (uint32_t)half * 2u * p.I;
+    const float4 s = p.sm_hs ? bf16_rows_dot<1, true>(row, 0u, p.sm_hs + 2u * t * p.I, nullptr, p.I / 8)
+                             : bf16_rows_dot<1, false>(row, 0u, 0u, p.shh + (size_t)t * 2 * p.I, p.I / 8);
+    if (lane == 0) ib[(size_t)t * DG + part * SDR + half] = s.x;
   }
 }
 
@@ -912,7 +914,7 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
             case I_SHGU_B: ns = 2 * min(SHP, p.I - it.a * SHP); break;
             case I_GU: ns = GT / GR; break;
             case I_SHDN: ns = z.dn_sh_parts; break;
-            case I_LOCAL: ns = NCW; break;
+            case I_LOCAL: ns = NPAIR; break;
             default: ns = n_exp; break;
           }
           const uint32_t islot = j % NIS;
@@ -1028,8 +1030,8 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     }
     if (lane == 0) {
       if (ok) {
-        // one stop per consumer warp
-        for (int s = 0; s < NCW; ++s) {
+        // one stop per consumer pair
+        for (int s = 0; s < NPAIR; ++s) {
           const uint32_t slot = n % NST, use = n / NST;
           if (use > 0 && !(ok = mbar_wait_bounded(bar(C.empty[slot]), (use - 1) & 1u, deadline, &p.ctrl->status)))
             break;
@@ -1047,62 +1049,79 @@ __global__ void __launch_bounds__(NTH, 1) k_decode_layer(const __grid_constant__
     }
   } else {
     // --------------------------------------------------------- consumers
+    // Warps 2i and 2i + 1 form pair i and work on one stage together: the
+    // leader takes the stage and waits for it, both run their half of the
+    // task, and after the pair's named barrier the leader releases the stage
+    // and counts the task (completing the item when it was the last).  Both
+    // warps leave the loop at the same stage, so the pair's barrier never
+    // waits for a warp that is gone.
+    const int pair = warp >> 1, pw = warp & 1, pbar_id = 1 + pair;
     for (;;) {
-      unsigned n = 0;
-      if (lane == 0) n = atomicAdd(&C.next, 1u);
-      n = __shfl_sync(0xffffffffu, n, 0);
-      const uint32_t slot = n % NST;
-      // A consumer can be more than one ring turn ahead of the stage it took
-      // (copies land out of order), where the parity of the full barrier
-      // alone would also match the stage's previous use: wait first until the
-      // producer has written this stage's header, then for the barrier.
-      bool got = true;
-      if (lane == 0) {
-        const volatile unsigned* seq = &C.hdr[slot].seq;
-        uint32_t spins = 0;
-        while (*seq != n) {
-          __nanosleep(32);
-          if ((++spins & 15u) == 0 && globaltimer_ns() > deadline) {
-            atomicOr(&p.ctrl->status, (unsigned)MOE_STATUS_TIMEOUT);
-            got = false;
-            break;
+      if (pw == 0) {
+        unsigned n = 0;
+        if (lane == 0) n = atomicAdd(&C.next, 1u);
+        n = __shfl_sync(0xffffffffu, n, 0);
+        const uint32_t slot = n % NST;
+        // A consumer can be more than one ring turn ahead of the stage it took
+        // (copies land out of order), where the parity of the full barrier
+        // alone would also match the stage's previous use: wait first until the
+        // producer has written this stage's header, then for the barrier.
+        bool got = true;
+        if (lane == 0) {
+          const volatile unsigned* seq = &C.hdr[slot].seq;
+          uint32_t spins = 0;
+          while (*seq != n) {
+            __nanosleep(32);
+            if ((++spins & 15u) == 0 && globaltimer_ns() > deadline) {
+              atomicOr(&p.ctrl->status, (unsigned)MOE_STATUS_TIMEOUT);
+              got = false;
+              break;
+            }
           }
+          if (got) got = mbar_wait_bounded(bar(C.full[slot]), (n / NST) & 1u, deadline, &p.ctrl->status);
+          C.pair_n[pair] = n;
+          C.pair_ok[pair] = got ? 1u : 0u;
         }
-        if (got) got = mbar_wait_bounded(bar(C.full[slot]), (n / NST) & 1u, deadline, &p.ctrl->status);
+        __syncwarp();
       }
-      got = __shfl_sync(0xffffffffu, got, 0);
-      if (!got) break;
+      named_bar_sync(pbar_id, 64);
+      const unsigned n = *reinterpret_cast<volatile unsigned*>(&C.pair_n[pair]);
+      if (!*reinterpret_cast<volatile unsigned*>(&C.pair_ok[pair])) break;
+      const uint32_t slot = n % NST;
       const Hdr h = C.hdr[slot];
       if (h.kind == K_STOP) break;
       const uint32_t st = slot * (uint32_t)SB;
       float* ib = item_buf(p, h.slot);
       switch (h.kind) {
-        case K_Q8: task_q8(p, h.a); break;
-        case K_ROUTER: task_router(p, C, st, h.a, deadline); break;
-        case K_SHGU_B: task_shgu_b(p, C, st, h.a, h.b, ib, deadline); break;
-        case K_LOCAL: task_local(p, C, h.a, deadline); break;
-        case K_GU_Q: task_gu_q(p, C, st, h.a, h.b, ib, deadline); break;
-        case K_DN_SHB: task_dn_b(p, C, st, h.a, ib, deadline); break;
+        case K_Q8: if (pw == 0) task_q8(p, h.a); break;
+        case K_ROUTER: if (pw == 0) task_router(p, C, st, h.a, deadline); break;
+        case K_SHGU_B: if (pw == 0) task_shgu_b(p, C, st, h.a, h.b, ib, deadline); break;
+        case K_LOCAL: task_local(p, C, 2 * h.a + pw, deadline); break;
+        case K_GU_Q: task_gu_q(p, C, st, h.a, h.b, ib, pw, deadline); break;
+        case K_DN_SHB: task_dn_b(p, C, st, h.a, ib, pw, deadline); break;
         case K_DN_SHQ:
-        case K_DN_RT: task_dn_q(p, C, st, h.kind == K_DN_RT ? h.a : -1, ib, deadline); break;
+        case K_DN_RT: task_dn_q(p, C, st, h.kind == K_DN_RT ? h.a : -1, ib, pw, deadline); break;
         default: break;
       }
-      // release the stage, then count the task against its item
+      // both halves are done with the stage: release it, then count the task
       __syncwarp();
       __threadfence_block();
-      unsigned left = 0;
-      if (lane == 0) {
-        mbar_arrive(bar(C.empty[slot]));
-        left = atomicSub(&C.item[h.slot].remaining, 1u);
-      }
-      left = __shfl_sync(0xffffffffu, left, 0);
-      if (left == 1u) {
-        __threadfence_block();
-        const Item it = C.item[h.slot];
-        complete_item(p, C, it, ib, deadline);
-        __syncwarp();
-        __threadfence_block();
-        if (lane == 0) mbar_arrive(bar(C.item_done[h.slot]));
+      named_bar_sync(pbar_id, 64);
+      if (pw == 0) {
+        unsigned left = 0;
+        if (lane == 0) {
+          mbar_arrive(bar(C.empty[slot]));
+          left = atomicSub(&C.item[h.slot].remaining, 1u);
+        }
+        left = __shfl_sync(0xffffffffu, left, 0);
+        if (left == 1u) {
+          __threadfence_block();
+          const Item it = C.item[h.slot];
+          complete_item(p, C, it, ib, deadline);
+          __syncwarp();
+          __threadfence_block();
+          if (lane == 0) mbar_arrive(bar(C.item_done[h.slot]));
+        }
       }
     }
   }
