@@ -1,7 +1,7 @@
 // Decode path (m <= 8): one fused persistent kernel per layer call.
 //
 // One block per SM: a producer warp, a planner warp and NCW consumer warps
-// around a ring of NST shared-memory stages.  The producer takes ITEMS by
+// (NPAIR pairs) around a ring of NST shared-memory stages.  The producer takes ITEMS by
 // ticket from four streams: first
 //   q8_1(x) | router rows | shared gate/up
 // then routed gate/up items as soon as its block's plan exists, shared down
@@ -53,7 +53,7 @@ constexpr int W_PROD = NCW;          // the producer warp
 constexpr int W_PLAN = NCW + 1;      // the planner warp: this block's copy of the routing
 constexpr int NTH = (NCW + 2) * 32;
 constexpr int SB = 13440;            // bytes per ring stage (4 + 4 Q2_K rows of 5120)
-constexpr int NST = 12;              // ring stages: NCW in work plus the copies in flight
+constexpr int NST = 12;              // ring stages: NPAIR in work plus the copies in flight
 constexpr int NIS = 4;               // item state slots
 constexpr int GR = 4;                // rows of W1 and of W3 per gate/up stage
 constexpr int GT = 32;               // rows per gate/up item (one q8_1 block of h)
@@ -235,9 +235,9 @@ __device__ __noinline__ float4 bf16_rows_dot(uint32_t w, uint32_t rs, uint32_t v
   return make_float4(o[0], o[1], o[2], o[3]);
 }
 
-// Four Q2_K rows (stage offset w, row stride rb) against one q8_1(x) vector
-// in the unit layout, by a half-warp (16 lanes, 1/16 of the units each).
-// Every lane of the half returns the four sums.
+// nr (at most four) Q2_K rows (stage offset w, row stride rb) against one
+// q8_1(x) vector in the unit layout, by a half-warp (16 lanes, 1/16 of the
+// units each).  Every lane of the half returns the sums (rows past nr: 0).
 template <bool S>
 __device__ __noinline__ float4 q2k_rows4_dot(uint32_t w, uint32_t rb, int nr, int U, uint32_t xs, const uint8_t* xg) {
   const int l = threadIdx.x & 15;
@@ -268,8 +268,8 @@ __device__ __noinline__ float4 q2k_rows4_dot(uint32_t w, uint32_t rb, int nr, in
   return make_float4(a0, a1, a2, a3);
 }
 
-// One Q3_K row (stage offset rowp) against one q8_1(h) vector, by the four
-// lanes of a row group (1/4 of the units each); the four lanes return the sum.
+// One Q3_K row (stage offset rowp) against one q8_1(h) vector, by the eight
+// lanes of a row group (1/8 of the units each); the eight lanes return the sum.
 template <bool S>
 __device__ __noinline__ float q3k_row_dot(uint32_t rowp, int U2, uint32_t hs, const uint8_t* hg) {
   const int q = threadIdx.x & 7;
@@ -557,9 +557,10 @@ __device__ __noinline__ void task_shgu_b(const DecodeParams& p, Ctl& C, uint32_t
   }
 }
 
-// GR rows of W1 (stage offset 0) and of W3 (offset GR*rb) in Q2_K against the
-// q8_1(x) units of the item's tokens: half-warp 0 takes W1, half-warp 1 W3.
-// h of the rows -> item buffer.
+// Rows 2 part, 2 part + 1 of the stage's GR rows of W1 (stage offset 0) and of
+// W3 (offset GR*rb) in Q2_K against the q8_1(x) units of the item's tokens
+// (part: this warp's half of the pair's task): half-warp 0 takes W1,
+// half-warp 1 W3.  h of the rows -> item buffer.
 __device__ __noinline__ void task_gu_q(const DecodeParams& p, Ctl& C, uint32_t st, int slot, int stg, float* ib,
                                        int part, uint64_t deadline) {
   const int lane = threadIdx.x & 31, half = lane >> 4;
@@ -593,8 +594,9 @@ __device__ __noinline__ void task_gu_q(const DecodeParams& p, Ctl& C, uint32_t s
   }
 }
 
-// DG rows of a Q3_K down matrix (stage offset st) against h units: lane =
-// (row, 1/4 of the units).  Routed (slot >= 0): E of each pair of the slot ->
+// Rows 4 part .. 4 part + 3 of the stage's DG rows of a Q3_K down matrix (stage
+// offset st; part: this warp's half of the pair's task) against h units: lane =
+// (row, 1/8 of the units).  Routed (slot >= 0): E of each pair of the slot ->
 // item buffer row pair*DG (unweighted); shared (slot < 0): the shared
 // expert's rows -> item buffer row t*DG.
 __device__ __noinline__ void task_dn_q(const DecodeParams& p, Ctl& C, uint32_t st, int slot, float* ib,
@@ -632,7 +634,9 @@ __device__ __noinline__ void task_dn_q(const DecodeParams& p, Ctl& C, uint32_t s
   }
 }
 
-// SDR rows of the bf16 shared down matrix against h (bf16 [m, I]) -> item buffer
+// Row `half` (this warp's half of the pair's task) of the stage's SDR rows of
+// the bf16 shared down matrix, part `part` of the group, against h (bf16
+// [m, I]) -> item buffer
 __device__ __noinline__ void task_dn_b(const DecodeParams& p, Ctl& C, uint32_t st, int part, float* ib,
                                        int half, uint64_t deadline) {
   const int lane = threadIdx.x & 31;
